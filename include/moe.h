@@ -1,0 +1,159 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse Mixture-of-Experts forward.
+ *
+ * The layer (after "Distributed Training Part 4: Tensor Parallelism, Hybrid Parallelism,
+ * MoE + Expert Parallelism", jesamkim ai-tech-blog, §3 Mixture of Experts and §4 Expert
+ * Parallelism):
+ *
+ *   z[t,e]    = (x[t] . W_r[e] + b_e) / tau                 router linear      (§3 Structure)
+ *   p[t,:]    = softmax(z[t,:])                              router softmax     (§3 Structure)
+ *   idx[t,:]  = the k largest z[t,e], descending, ties to the lower e           (§3 TopK)
+ *   gate[t,j] = p[t, idx[t,j]]   (not renormalised)                              (§3 G(x)_i)
+ *   dispatch  = rows (t,j) in expert-contiguous order, stable in token order     (§4 Dispatch)
+ *   E_e(v)    = W2_e (SiLU(W1_e v) * (W3_e v))             SwiGLU expert FFN  (§3 "FFN")
+ *   y[t]      = sum_j gate[t,j] * E_{idx[t,j]}(x[t])         combine            (§3 output, §4 Combine)
+ *   aux       = E * sum_e f_e P_e,  f_e = count_e/(T k),  P_e = mean_t p[t,e]  (§3 Load-Balancing Loss)
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers unless the name ends in _host.  All are
+ *     row-major and contiguous: x [T,d]; W_r [E,d]; router bias [E] fp32; W1, W3 [E,F,d]
+ *     (row f of expert e is the weight vector of hidden unit f); W2 [E,d,F]; y [T,d].
+ *     x, W_r, W1, W3, W2 have the plan's act_dtype; y has its out_dtype.
+ *   - Device pointers must be 16-byte aligned, the workspace 256-byte aligned;
+ *     otherwise MOE_ERR_INVALID_ARG.
+ *   - The caller owns all device memory, the workspace included.  The library owns only
+ *     the host-side plan object; a plan holds no device memory and may be used from one
+ *     thread at a time.
+ *   - Every call that takes a stream (a cudaStream_t passed as void*, NULL = legacy default
+ *     stream) only enqueues work on it: no allocation, no synchronisation, unless its
+ *     comment says otherwise.  Workspace contents are defined once the stream reaches the
+ *     point after the call.
+ *   - Errors are returned as moe_status; nothing is thrown across the ABI.  A CUDA error
+ *     from an enqueue maps to MOE_ERR_CUDA; moe_last_error() then describes it.
+ *   - Device-side waits are bounded: a kernel that waits longer than the plan's
+ *     wait_timeout_ns records MOE_ERR_TIMEOUT in the workspace's status word and returns;
+ *     moe_get_device_status() reports it.  No kernel traps.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or config value */
+  MOE_ERR_UNSUPPORTED = 2, /* valid config this build does not handle (e.g. bf16 with d % 64 != 0) */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  MOE_ERR_TIMEOUT = 4,     /* a device-side wait ran out (reported by moe_get_device_status) */
+  MOE_ERR_INTERNAL = 5     /* a device-side consistency check failed */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Which kernels run the router and the expert GEMMs.
+ *   MOE_PATH_AUTO: bf16 -> tcgen05/TMEM/TMA kernels; fp32 -> fp32 SIMT kernels (true fp32).
+ *   MOE_PATH_SIMT: SIMT kernels for every dtype (fp32 FMA, a cross-check of the tensor path). */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_SIMT = 1 } moe_path;
+
+/* flags */
+#define MOE_FLAG_KEEP_LOGITS 1u /* the router also stores its fp32 logits z [T,E] in the workspace */
+#define MOE_FLAG_TEST_STALL 2u  /* test hook: the expert-GEMM producer withholds its first stage,
+                                   so its consumers' bounded waits run out (MOE_ERR_TIMEOUT) */
+
+typedef struct {
+  int64_t T;                /* tokens, >= 1 */
+  int32_t d_model;          /* d, >= 1 */
+  int32_t n_experts;        /* E, 1..256 */
+  int32_t top_k;            /* k, 1..min(E, 8) */
+  int32_t d_expert;         /* F, >= 1 */
+  int32_t act_dtype;        /* moe_dtype of x, W_r, W1, W3, W2 */
+  int32_t out_dtype;        /* moe_dtype of y */
+  float router_temperature; /* tau > 0 */
+  int32_t has_router_bias;  /* 0/1: moe_forward reads a bias [E] (fp32) */
+  int32_t path;             /* moe_path */
+  uint32_t flags;           /* MOE_FLAG_* */
+  int64_t wait_timeout_ns;  /* bound on any device-side wait; <= 0 selects 2 s */
+} moe_config;
+
+typedef struct moe_plan_s* moe_plan_t;
+
+/* Device pointers into a workspace, for inspecting the intermediates of the last forward
+ * run on it.  N = T*k routed rows; "row p" is the p-th row in expert-contiguous order. */
+typedef struct {
+  uint32_t* status;        /* status word: 0 or a moe_status recorded by a kernel */
+  float* aux;              /* balancing scalar (fp32) */
+  int32_t* topk_idx;       /* [T,k] chosen experts, descending logit */
+  float* topk_gate;        /* [T,k] gates = softmax entries at topk_idx */
+  int32_t* expert_counts;  /* [E] rows per expert */
+  int32_t* expert_offsets; /* [E+1] exclusive scan of expert_counts */
+  int32_t* perm_src;       /* [N] token of row p */
+  int32_t* perm_slot;      /* [N] slot t*k+j of row p */
+  float* gate_perm;        /* [N] gate of row p */
+  int32_t* slot_pos;       /* [N] row p of slot t*k+j */
+  float* logits;           /* [T,E] router logits, or NULL unless MOE_FLAG_KEEP_LOGITS */
+  void* xp;                /* [N,d] act dtype: x rows in dispatch order */
+  void* h;                 /* [N,F] act dtype: SwiGLU hidden rows */
+  void* yslot;             /* [T*k,d] act dtype: gate * expert output, token-slot order */
+} moe_views;
+
+/* Build a plan for one layer shape (host only; no device work).  Validates the config
+ * (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED), chooses kernels and tile shapes, and
+ * returns in *workspace_bytes the size of the device workspace every forward needs. */
+moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_bytes);
+
+/* Release a plan (NULL is ignored). */
+void moe_plan_destroy(moe_plan_t plan);
+
+/* The whole forward on `stream`: router, top-k, histogram/scan, dispatch, grouped
+ * SwiGLU GEMM, grouped down-projection with gate and un-permute, combine, and the
+ * balancing scalar (left in the workspace).  router_bias may be NULL only when the plan
+ * has has_router_bias = 0.  y is written completely.  Asynchronous. */
+moe_status moe_forward(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
+                       const void* w1, const void* w3, const void* w2, void* y, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Number of kernel stages moe_forward enqueues, and their names. */
+int32_t moe_stage_count(moe_plan_t plan);
+const char* moe_stage_name(moe_plan_t plan, int32_t stage);
+
+/* Enqueue only stage `stage` (0 <= stage < moe_stage_count) of moe_forward, with the same
+ * arguments.  Running stages 0..n-1 in order on one stream is exactly moe_forward; this
+ * lets a caller place timing events between the kernels. */
+moe_status moe_forward_stage(moe_plan_t plan, int32_t stage, const void* x, const void* w_router,
+                             const float* router_bias, const void* w1, const void* w3, const void* w2,
+                             void* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The forward with host activations: copies x_host -> x_dev, runs moe_forward(x_dev ... y_dev),
+ * copies y_dev -> y_host, all on `stream` (cudaMemcpyAsync; pinned host buffers make the
+ * copies asynchronous).  The weights stay device-resident.  The caller synchronises the
+ * stream before reading y_host. */
+moe_status moe_forward_host(moe_plan_t plan, const void* x_host, void* x_dev, const void* w_router,
+                            const float* router_bias, const void* w1, const void* w3, const void* w2,
+                            void* y_dev, void* y_host, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Copy the balancing scalar aux = E * sum_e f_e P_e of the last forward on `workspace`
+ * to the device float *aux_out (stream-ordered, asynchronous).  (§3 Load-Balancing Loss) */
+moe_status moe_aux_loss(moe_plan_t plan, const void* workspace, float* aux_out, void* stream);
+
+/* Fill *views with pointers into `workspace` (host only, no device access). */
+moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* views);
+
+/* SYNCHRONISES `stream`, then reads the workspace's status word: MOE_OK, or the error a
+ * kernel of the last forward recorded (MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL), or MOE_ERR_CUDA
+ * if the synchronisation itself failed.  Each moe_forward clears the word first. */
+moe_status moe_get_device_status(moe_plan_t plan, const void* workspace, void* stream);
+
+/* Text of a status code, and a description of the last error on this thread. */
+const char* moe_status_string(moe_status s);
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

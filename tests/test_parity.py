@@ -1,0 +1,151 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small shapes are checked in full (every token, every routed row of Xp, sampled rows of H,
+every y).  The five listed workloads are checked at full size in the launch configuration
+the benchmark uses: routing, gates, dispatch, Xp and aux on every token, H and y on
+seeded samples (plus every token of the smallest non-empty expert).
+"""
+import numpy as np
+import pytest
+import torch
+
+from top_routing_grouped_gb300.workloads import SHAPES, ORDER, MoEShape, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ["auto", "simt"]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from top_routing_grouped_gb300 import moe as m
+    return m
+
+
+def small(name, T, d, E, k, F, dtype="bf16", tau=1.0):
+    return MoEShape(name, T=T, d=d, E=E, k=k, F=F, dtype=dtype, tau=tau)
+
+
+def check(moe, shape, inputs, path="auto", y_tokens=None, h_rows=None, has_bias=None):
+    import parity
+    plan = moe.MoEPlan(shape.T, shape.d, shape.E, shape.k, shape.F, dtype=shape.dtype, tau=shape.tau,
+                       has_bias=(inputs.bias is not None) if has_bias is None else has_bias,
+                       path=path, keep_logits=True)
+    rep, got = parity.full_check(shape, inputs, plan, y_tokens=y_tokens, h_rows=h_rows)
+    print(f"\n[{shape.name} path={path}]\n{rep}")
+    return rep, got
+
+
+def test_tiny_f32_full(moe):
+    s = SHAPES["tiny_f32"]
+    check(moe, s, make_inputs(s, seed=0))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dims", [
+    (300, 256, 8, 2, 192),    # ragged T (not a multiple of the 128-token blocks), 3 n-tiles
+    (1, 128, 8, 2, 128),      # a single token
+    (257, 128, 1, 1, 64),     # E = 1, k = 1: a dense SwiGLU FFN
+    (130, 192, 4, 4, 128),    # k = E: every expert on every token
+    (512, 128, 16, 8, 320),   # k = 8 (the largest), F not a power of two
+    (40, 64, 64, 2, 64),      # more experts than routed rows per expert: counts of 0, 1, 2
+], ids=lambda d: "x".join(map(str, d)))
+def test_small_bf16(moe, path, dims):
+    T, d, E, k, F = dims
+    s = small("small", T, d, E, k, F)
+    check(moe, s, make_inputs(s, seed=1), path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_temperature_and_bias(moe, path):
+    s = small("tau_bias", 384, 256, 16, 4, 128, tau=0.5)
+    inp = make_inputs(s, seed=2)
+    inp.bias = torch.linspace(-1.0, 1.0, s.E, dtype=torch.float32)
+    check(moe, s, inp, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_all_tokens_to_one_expert(moe, path):
+    """A +100 logit bias on expert 0: every token routes its first slot there."""
+    s = small("collapse", 300, 128, 8, 2, 128)
+    inp = make_inputs(s, seed=3)
+    inp.bias = torch.zeros(s.E, dtype=torch.float32)
+    inp.bias[0] = 100.0
+    rep, got = check(moe, s, inp, path=path)
+    idx = got["views"]["topk_idx"].cpu()
+    assert torch.all(idx[:, 0] == 0)
+    assert got["views"]["expert_counts"][0].item() == s.T
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_uniform_router_aux_is_one(moe, path):
+    """W_r = 0: every logit equal, p = 1/E; the balancing scalar is exactly 1 (k slots
+    always sum to 1 whatever the tie-break) and top-k takes the lowest indices."""
+    s = small("uniform", 256, 128, 8, 2, 64)
+    inp = make_inputs(s, seed=4)
+    inp.w_router = torch.zeros_like(inp.w_router)
+    rep, got = check(moe, s, inp, path=path)
+    assert abs(got["aux"] - 1.0) <= 1e-6
+    assert torch.all(got["views"]["topk_idx"].cpu() == torch.tensor([0, 1], dtype=torch.int32))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_out_dtype_f32(moe, path):
+    import parity
+    s = small("outf32", 200, 128, 8, 2, 128)
+    inp = make_inputs(s, seed=5)
+    plan = moe.MoEPlan(s.T, s.d, s.E, s.k, s.F, dtype="bf16", out_dtype="f32", path=path)
+    got = parity.run_gpu(plan, inp.to("cuda"))
+    plan_b = moe.MoEPlan(s.T, s.d, s.E, s.k, s.F, dtype="bf16", path=path)
+    got_b = parity.run_gpu(plan_b, inp.to("cuda"))
+    assert got["y"].dtype == torch.float32
+    # same arithmetic; only the final rounding differs
+    assert torch.allclose(got["y"].bfloat16().float(), got_b["y"].float(), atol=0, rtol=0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_deterministic(moe, path):
+    import parity
+    s = small("det", 640, 256, 16, 4, 256)
+    dev = make_inputs(s, seed=6).to("cuda")
+    plan = moe.MoEPlan(s.T, s.d, s.E, s.k, s.F, path=path)
+    a = parity.run_gpu(plan, dev)
+    b = parity.run_gpu(plan, dev)
+    assert torch.equal(a["y"], b["y"])
+    assert a["aux"] == b["aux"]
+
+
+def smallest_expert_tokens(got, cap=48):
+    v = got["views"]
+    counts = v["expert_counts"].cpu().numpy()
+    off = v["expert_offsets"].cpu().numpy()
+    nz = np.where(counts > 0)[0]
+    e = nz[np.argmin(counts[nz])]
+    return v["perm_src"].cpu().numpy()[off[e]:off[e + 1]][:cap]
+
+
+@pytest.mark.parametrize("name", ORDER[1:])
+@pytest.mark.parametrize("path", ["auto"])
+def test_full_size_workloads(moe, name, path):
+    """The listed workloads at full size: every token's routing and dispatch, sampled H
+    rows and y tokens."""
+    import parity
+    s = SHAPES[name]
+    inp = make_inputs(s, seed=0)
+    rng = np.random.default_rng(0)
+    toks = np.unique(rng.integers(0, s.T, size=48))
+    N = s.T * s.k
+    rows = np.unique(np.concatenate([rng.integers(0, N, size=32), [0, N - 1]]))
+    plan = moe.MoEPlan.for_shape(s, path=path, keep_logits=True)
+    rep, got = parity.full_check(s, inp, plan, y_tokens=toks, h_rows=rows)
+    orc_tokens = smallest_expert_tokens(got)
+    import oracle
+    host = inp.numpy_for_oracle()
+    orc = oracle.Oracle(s.T, s.d, s.E, s.k, s.F, tau=s.tau, dtype=s.dtype)
+    z, p, _, _ = orc.router(host["x"], host["wr"], host["bias"])
+    gidx = got["views"]["topk_idx"].cpu().numpy()
+    gref = np.take_along_axis(p, gidx, axis=1)
+    parity.check_y(orc, host, got, gidx, gref, orc_tokens, parity.Y_TOL[s.dtype], rep)
+    print(f"\n[{name} path={path}]\n{rep}")
+    if name == "skewed_e128":
+        assert (got["views"]["expert_counts"] == 0).sum().item() >= 1

@@ -1,0 +1,352 @@
+// api.cu -- the C ABI (include/moe.h): plan validation, workspace layout, and the launch
+// sequence of the forward.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+
+#include "moe_internal.h"
+#include "gemm_tc.h"
+
+struct moe_plan_s {
+  moe_config cfg;
+  moe::Shape shape;
+  moe::WsLayout layout;
+  bool tc;          // tensor-core router and expert GEMMs (bf16 layers on MOE_PATH_AUTO)
+  int device = -1;  // device the cached attributes belong to
+  int num_sms = 0;
+  int64_t timeout_ns;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr const char* kStageNames[] = {"route", "scan", "permute", "gemm1_swiglu", "gemm2_gate", "combine"};
+constexpr int kNumStages = 6;
+
+// Attributes of the current device, cached on the plan.
+moe_status bind_device(moe_plan_t plan) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev == plan->device) return MOE_OK;
+  int sms = 0, major = 0, minor = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (plan->tc && !(major == 10 && minor == 3))
+    return fail(MOE_ERR_UNSUPPORTED, "tensor-core path needs an sm_103 device, found sm_%d%d", major, minor);
+  plan->device = dev;
+  plan->num_sms = sms;
+  return MOE_OK;
+}
+
+}  // namespace
+
+namespace moe {
+
+WsLayout ws_layout(const Shape& s) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  const size_t esz = s.act_bf16 ? 2 : 4;
+  const size_t N = (size_t)s.N, E = (size_t)s.E, nb = (size_t)s.nblk;
+  L.hdr = take(64 * sizeof(uint32_t));
+  L.aux = take(sizeof(float));
+  L.blk_cnt = take(nb * E * 4);
+  L.blk_psum = take(nb * E * 4);
+  L.local_rank = take(N * 4);
+  L.topk_idx = take(N * 4);
+  L.topk_gate = take(N * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.blk_base = take(nb * E * 4);
+  L.grp_expert = take((size_t)s.max_groups * 4);
+  L.grp_mtile0 = take((size_t)s.max_groups * 4);
+  L.grp_mpre = take(((size_t)s.max_groups + 1) * 4);
+  L.perm_src = take(N * 4);
+  L.perm_slot = take(N * 4);
+  L.gate_perm = take(N * 4);
+  L.slot_pos = take(N * 4);
+  L.logits = s.keep_logits ? take((size_t)s.T * E * 4) : 0;
+  L.xp = take(N * (size_t)s.d * esz);
+  L.h = take(N * (size_t)s.F * esz);
+  L.yslot = take(N * (size_t)s.d * esz);
+  L.total = off;
+  return L;
+}
+
+Ws ws_bind(const Shape& s, void* base) {
+  const WsLayout L = ws_layout(s);
+  char* b = static_cast<char*>(base);
+  Ws w{};
+  w.hdr = reinterpret_cast<uint32_t*>(b + L.hdr);
+  w.aux = reinterpret_cast<float*>(b + L.aux);
+  w.blk_cnt = reinterpret_cast<int32_t*>(b + L.blk_cnt);
+  w.blk_psum = reinterpret_cast<float*>(b + L.blk_psum);
+  w.local_rank = reinterpret_cast<int32_t*>(b + L.local_rank);
+  w.topk_idx = reinterpret_cast<int32_t*>(b + L.topk_idx);
+  w.topk_gate = reinterpret_cast<float*>(b + L.topk_gate);
+  w.counts = reinterpret_cast<int32_t*>(b + L.counts);
+  w.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  w.blk_base = reinterpret_cast<int32_t*>(b + L.blk_base);
+  w.grp_expert = reinterpret_cast<int32_t*>(b + L.grp_expert);
+  w.grp_mtile0 = reinterpret_cast<int32_t*>(b + L.grp_mtile0);
+  w.grp_mpre = reinterpret_cast<int32_t*>(b + L.grp_mpre);
+  w.perm_src = reinterpret_cast<int32_t*>(b + L.perm_src);
+  w.perm_slot = reinterpret_cast<int32_t*>(b + L.perm_slot);
+  w.gate_perm = reinterpret_cast<float*>(b + L.gate_perm);
+  w.slot_pos = reinterpret_cast<int32_t*>(b + L.slot_pos);
+  w.logits = s.keep_logits ? reinterpret_cast<float*>(b + L.logits) : nullptr;
+  w.xp = b + L.xp;
+  w.h = b + L.h;
+  w.yslot = b + L.yslot;
+  return w;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_INTERNAL: return "MOE_ERR_INTERNAL";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_bytes) {
+  if (!cfg || !plan || !workspace_bytes) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  *plan = nullptr;
+  const moe_config& c = *cfg;
+  if (c.T < 1 || c.d_model < 1 || c.d_expert < 1) return fail(MOE_ERR_INVALID_ARG, "T, d_model, d_expert must be >= 1");
+  if (c.n_experts < 1 || c.n_experts > moe::kMaxExperts)
+    return fail(MOE_ERR_INVALID_ARG, "n_experts must be in [1, %d]", moe::kMaxExperts);
+  if (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > moe::kMaxTopK)
+    return fail(MOE_ERR_INVALID_ARG, "top_k must be in [1, min(n_experts, %d)]", moe::kMaxTopK);
+  if (c.act_dtype != MOE_F32 && c.act_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "bad act_dtype");
+  if (c.out_dtype != MOE_F32 && c.out_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "bad out_dtype");
+  if (!(c.router_temperature > 0.f) || !isfinite(c.router_temperature))
+    return fail(MOE_ERR_INVALID_ARG, "router_temperature must be finite and > 0");
+  if (c.has_router_bias != 0 && c.has_router_bias != 1) return fail(MOE_ERR_INVALID_ARG, "has_router_bias must be 0 or 1");
+  if (c.path != MOE_PATH_AUTO && c.path != MOE_PATH_SIMT) return fail(MOE_ERR_INVALID_ARG, "bad path");
+  if (c.flags & ~(MOE_FLAG_KEEP_LOGITS | MOE_FLAG_TEST_STALL)) return fail(MOE_ERR_INVALID_ARG, "unknown flags");
+  const int64_t N = c.T * (int64_t)c.top_k;
+  if (N > (int64_t)INT32_MAX / 2 || N * (int64_t)(c.d_model > c.d_expert ? c.d_model : c.d_expert) > ((int64_t)1 << 40))
+    return fail(MOE_ERR_UNSUPPORTED, "T * top_k (or the routed activations) too large");
+  const bool bf16 = c.act_dtype == MOE_BF16;
+  const bool tc = bf16 && c.path == MOE_PATH_AUTO && moe::kTensorCorePathBuilt;
+  if (!bf16 && c.d_model % 4 != 0) return fail(MOE_ERR_UNSUPPORTED, "fp32 layers need d_model %% 4 == 0");
+  if (bf16 && c.d_model % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "bf16 layers need d_model %% 8 == 0");
+  if (tc && (c.d_model % 64 != 0 || c.d_expert % 64 != 0))
+    return fail(MOE_ERR_UNSUPPORTED, "the tensor-core path needs d_model and d_expert multiples of 64 (use MOE_PATH_SIMT)");
+  if ((c.flags & MOE_FLAG_TEST_STALL) && !tc)
+    return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_TEST_STALL applies to the tensor-core path only");
+
+  moe_plan_s* p = new (std::nothrow) moe_plan_s();
+  if (!p) return fail(MOE_ERR_INTERNAL, "out of host memory");
+  p->cfg = c;
+  moe::Shape& s = p->shape;
+  s.T = c.T;
+  s.N = N;
+  s.d = c.d_model;
+  s.E = c.n_experts;
+  s.k = c.top_k;
+  s.F = c.d_expert;
+  s.nblk = (int)((c.T + moe::kRouteBlock - 1) / moe::kRouteBlock);
+  s.tau = c.router_temperature;
+  s.has_bias = c.has_router_bias;
+  s.keep_logits = (c.flags & MOE_FLAG_KEEP_LOGITS) ? 1 : 0;
+  s.act_bf16 = bf16 ? 1 : 0;
+  s.out_bf16 = c.out_dtype == MOE_BF16 ? 1 : 0;
+  // groups of up to kGroupM m-tiles per expert: sum_e ceil(mt_e / G) <= MT / G + E and
+  // MT = sum_e ceil(count_e / 128) <= N / 128 + E
+  s.max_groups = (int)(N / ((int64_t)moe::kTileM * moe::kGroupM) + 2 * (int64_t)c.n_experts + 2);
+  p->layout = moe::ws_layout(s);
+  p->tc = tc;
+  p->timeout_ns = c.wait_timeout_ns > 0 ? c.wait_timeout_ns : 2000000000LL;
+  *plan = p;
+  *workspace_bytes = p->layout.total;
+  g_last_error.clear();
+  return MOE_OK;
+}
+
+void moe_plan_destroy(moe_plan_t plan) { delete plan; }
+
+int32_t moe_stage_count(moe_plan_t plan) { return plan ? kNumStages : 0; }
+
+const char* moe_stage_name(moe_plan_t plan, int32_t stage) {
+  if (!plan || stage < 0 || stage >= kNumStages) return nullptr;
+  return kStageNames[stage];
+}
+
+static moe_status check_forward_args(moe_plan_t plan, const void* x, const void* w_router, const float* bias,
+                                     const void* w1, const void* w3, const void* w2, void* y, void* workspace,
+                                     size_t workspace_bytes) {
+  if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+  const void* ptrs[] = {x, w_router, w1, w3, w2, y};
+  const char* names[] = {"x", "w_router", "w1", "w3", "w2", "y"};
+  for (int i = 0; i < 6; ++i) {
+    if (!ptrs[i]) return fail(MOE_ERR_INVALID_ARG, "%s is null", names[i]);
+    if (!aligned(ptrs[i], 16)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  if (plan->shape.has_bias && (!bias || !aligned(bias, 16)))
+    return fail(MOE_ERR_INVALID_ARG, "router_bias must be a 16-byte aligned pointer (plan has a bias)");
+  if (!workspace || !aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan->layout.total)
+    return fail(MOE_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, plan->layout.total);
+  return MOE_OK;
+}
+
+static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& w, void* workspace, cudaStream_t st) {
+  const moe::Shape& s = plan->shape;
+  const moe::Ws ws = moe::ws_bind(s, workspace);
+  cudaError_t e = cudaSuccess;
+  switch (stage) {
+    case 0:
+      e = cudaMemsetAsync(ws.hdr, 0, 4 * sizeof(uint32_t), st);
+      if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+      e = plan->tc ? moe::launch_route_tc(s, ws, w, st) : moe::launch_route_simt(s, ws, w, st);
+      break;
+    case 1: e = moe::launch_scan(s, ws, st); break;
+    case 2: e = moe::launch_permute(s, ws, w, plan->num_sms, st); break;
+    case 3:
+      e = plan->tc ? moe::launch_gemm_tc(1, s, ws, w, plan->num_sms, plan->timeout_ns,
+                                         (plan->cfg.flags & MOE_FLAG_TEST_STALL) != 0, st)
+                   : moe::launch_gemm1_simt(s, ws, w, plan->num_sms, st);
+      break;
+    case 4:
+      e = plan->tc ? moe::launch_gemm_tc(2, s, ws, w, plan->num_sms, plan->timeout_ns, false, st)
+                   : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, st);
+      break;
+    case 5: e = moe::launch_combine(s, ws, w, plan->num_sms, st); break;
+    default: return fail(MOE_ERR_INVALID_ARG, "stage %d out of range", stage);
+  }
+  if (e != cudaSuccess) {
+    char what[64];
+    snprintf(what, sizeof what, "launching stage %s", kStageNames[stage]);
+    return cuda_fail(e, what);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_forward_stage(moe_plan_t plan, int32_t stage, const void* x, const void* w_router,
+                             const float* router_bias, const void* w1, const void* w3, const void* w2, void* y,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status st = check_forward_args(plan, x, w_router, router_bias, w1, w3, w2, y, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if ((st = bind_device(plan)) != MOE_OK) return st;
+  const moe::Weights w{x, w_router, plan->shape.has_bias ? router_bias : nullptr, w1, w3, w2, y};
+  return run_stage(plan, stage, w, workspace, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
+                       const void* w1, const void* w3, const void* w2, void* y, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  moe_status st = check_forward_args(plan, x, w_router, router_bias, w1, w3, w2, y, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if ((st = bind_device(plan)) != MOE_OK) return st;
+  const moe::Weights w{x, w_router, plan->shape.has_bias ? router_bias : nullptr, w1, w3, w2, y};
+  for (int i = 0; i < kNumStages; ++i)
+    if ((st = run_stage(plan, i, w, workspace, static_cast<cudaStream_t>(stream))) != MOE_OK) return st;
+  return MOE_OK;
+}
+
+moe_status moe_forward_host(moe_plan_t plan, const void* x_host, void* x_dev, const void* w_router,
+                            const float* router_bias, const void* w1, const void* w3, const void* w2, void* y_dev,
+                            void* y_host, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || !x_host || !y_host) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  moe_status st = check_forward_args(plan, x_dev, w_router, router_bias, w1, w3, w2, y_dev, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  const moe::Shape& s = plan->shape;
+  const size_t xbytes = (size_t)s.T * s.d * (s.act_bf16 ? 2 : 4);
+  const size_t ybytes = (size_t)s.T * s.d * (s.out_bf16 ? 2 : 4);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "copying x to the device");
+  if ((st = moe_forward(plan, x_dev, w_router, router_bias, w1, w3, w2, y_dev, workspace, workspace_bytes, stream)) != MOE_OK)
+    return st;
+  e = cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "copying y to the host");
+  return MOE_OK;
+}
+
+moe_status moe_aux_loss(moe_plan_t plan, const void* workspace, float* aux_out, void* stream) {
+  if (!plan || !workspace || !aux_out) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const char* src = static_cast<const char*>(workspace) + plan->layout.aux;
+  cudaError_t e = cudaMemcpyAsync(aux_out, src, sizeof(float), cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copying aux");
+  return MOE_OK;
+}
+
+moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* v) {
+  if (!plan || !workspace || !v) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  const moe::Ws w = moe::ws_bind(plan->shape, workspace);
+  v->status = w.hdr + moe::kHdrStatus;
+  v->aux = w.aux;
+  v->topk_idx = w.topk_idx;
+  v->topk_gate = w.topk_gate;
+  v->expert_counts = w.counts;
+  v->expert_offsets = w.offsets;
+  v->perm_src = w.perm_src;
+  v->perm_slot = w.perm_slot;
+  v->gate_perm = w.gate_perm;
+  v->slot_pos = w.slot_pos;
+  v->logits = w.logits;
+  v->xp = w.xp;
+  v->h = w.h;
+  v->yslot = w.yslot;
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(moe_plan_t plan, const void* workspace, void* stream) {
+  if (!plan || !workspace) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "synchronising the stream");
+  uint32_t hdr[2] = {0, 0};
+  e = cudaMemcpy(hdr, static_cast<const char*>(workspace) + plan->layout.hdr, sizeof hdr, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (hdr[0] == 0) return MOE_OK;
+  if (hdr[0] == MOE_ERR_TIMEOUT || hdr[0] == MOE_ERR_INTERNAL)
+    return fail((moe_status)hdr[0], "device reported %s at site 0x%x", moe_status_string((moe_status)hdr[0]), hdr[1]);
+  return fail(MOE_ERR_INTERNAL, "device status word holds unknown value %u", hdr[0]);
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// combine.cu -- y[t] = sum_{j<k} Yslot[t*k + j], in j order, fp32 accumulation.
+//
+// After "Distributed Training Part 4 ... MoE + Expert Parallelism" (jesamkim ai-tech-blog),
+// §3 output formula y = sum_{i in TopK} G(x)_i E_i(x) (the gate factor is already applied
+// by the down-projection epilogue) and §4 Combine (expert outputs return to their token).
+// A fixed summation order keeps y bit-reproducible (no float atomics).
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+
+namespace moe {
+
+constexpr int kCombThreads = 256;
+
+// bf16 slots -> bf16 or fp32 y; 8 columns (one 16-byte load per slot) per thread-step.
+template <bool kOutBf16>
+__global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws ws, Weights w) {
+  const int vec_per_row = s.d / 8;
+  const int64_t total = s.T * (int64_t)vec_per_row;
+  const int4* ys = reinterpret_cast<const int4*>(ws.yslot);
+  for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * kCombThreads) {
+    const int64_t t = i / vec_per_row;
+    const int v = (int)(i % vec_per_row);
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int j = 0; j < s.k; ++j) {
+      int4 raw = __ldcs(ys + (t * s.k + j) * vec_per_row + v);
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h2[q]);
+        acc[2 * q] += f.x;
+        acc[2 * q + 1] += f.y;
+      }
+    }
+    if constexpr (kOutBf16) {
+      int4 out;
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o2[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      reinterpret_cast<int4*>(w.y)[t * vec_per_row + v] = out;
+    } else {
+      float4* yo = reinterpret_cast<float4*>(w.y) + (t * vec_per_row + v) * 2;
+      yo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+
+// fp32 slots -> fp32 or bf16 y; 4 columns per thread-step.
+template <bool kOutBf16>
+__global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws ws, Weights w) {
+  const int vec_per_row = s.d / 4;
+  const int64_t total = s.T * (int64_t)vec_per_row;
+  const float4* ys = reinterpret_cast<const float4*>(ws.yslot);
+  for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * kCombThreads) {
+    const int64_t t = i / vec_per_row;
+    const int v = (int)(i % vec_per_row);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < s.k; ++j) {
+      const float4 f = ys[(t * s.k + j) * vec_per_row + v];
+      acc.x += f.x;
+      acc.y += f.y;
+      acc.z += f.z;
+      acc.w += f.w;
+    }
+    if constexpr (kOutBf16) {
+      __nv_bfloat162* yo = reinterpret_cast<__nv_bfloat162*>(w.y) + (t * vec_per_row + v) * 2;
+      yo[0] = __floats2bfloat162_rn(acc.x, acc.y);
+      yo[1] = __floats2bfloat162_rn(acc.z, acc.w);
+    } else {
+      reinterpret_cast<float4*>(w.y)[t * vec_per_row + v] = acc;
+    }
+  }
+}
+
+cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st) {
+  const int64_t per = s.act_bf16 ? 8 : 4;
+  int64_t blocks = (s.T * (s.d / per) + kCombThreads - 1) / kCombThreads;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (s.act_bf16) {
+    if (s.out_bf16) combine_bf16_kernel<true><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
+    else combine_bf16_kernel<false><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
+  } else {
+    if (s.out_bf16) combine_f32_kernel<true><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
+    else combine_f32_kernel<false><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

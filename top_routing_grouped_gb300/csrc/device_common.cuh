@@ -1,0 +1,66 @@
+// device_common.cuh -- small device helpers shared by the kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ float load_act(const void* base, int bf16, int64_t i) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+  return reinterpret_cast<const float*>(base)[i];
+}
+
+__device__ __forceinline__ void store_act(void* base, int bf16, int64_t i, float v) {
+  if (bf16)
+    reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(base)[i] = v;
+}
+
+// First error wins; `where` records which kernel/site saw it.
+__device__ __forceinline__ void record_error(const Ws& ws, uint32_t code, uint32_t where) {
+  if (atomicCAS(&ws.hdr[kHdrStatus], 0u, code) == 0u) ws.hdr[kHdrWhere] = where;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One m x n output tile of a grouped GEMM.
+struct TileInfo {
+  int e;      // expert
+  int row0;   // first row in dispatch order
+  int rows;   // valid rows (1..kTileM)
+  int n_idx;  // n-tile index
+};
+
+// Decode linear tile id -> tile.  Scheduling groups hold up to kGroupM consecutive
+// m-tiles of one expert; inside a group the m-tile index runs fastest, so CTAs that run
+// at the same time share the same weight n-tile (read once from HBM, then from L2).
+// Group g owns tiles [n_tiles * mpre[g], n_tiles * mpre[g+1]).
+__device__ __forceinline__ TileInfo decode_tile(const Ws& ws, int ngroups, int n_tiles, int tile) {
+  const int q = tile / n_tiles;
+  int lo = 0, hi = ngroups - 1;  // largest g with mpre[g] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&ws.grp_mpre[mid]) <= q) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int m_begin = __ldg(&ws.grp_mpre[g]);
+  const int gm = __ldg(&ws.grp_mpre[g + 1]) - m_begin;
+  const int local = tile - n_tiles * m_begin;
+  TileInfo ti;
+  ti.e = __ldg(&ws.grp_expert[g]);
+  ti.n_idx = local / gm;
+  const int mt = __ldg(&ws.grp_mtile0[g]) + local % gm;
+  ti.row0 = __ldg(&ws.offsets[ti.e]) + mt * kTileM;
+  const int rem = __ldg(&ws.counts[ti.e]) - mt * kTileM;
+  ti.rows = rem < kTileM ? rem : kTileM;
+  return ti;
+}
+
+}  // namespace moe

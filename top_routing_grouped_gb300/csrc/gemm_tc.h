@@ -1,0 +1,15 @@
+// gemm_tc.h -- tensor-core (tcgen05 / TMEM / TMA) kernels for sm_103a.
+#pragma once
+#include "moe_internal.h"
+
+namespace moe {
+
+// False until the tcgen05 kernels are in place; the plan then routes bf16 layers there.
+constexpr bool kTensorCorePathBuilt = false;
+
+cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st);
+// mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yslot[slot] = gate * (H W2^T)
+cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
+                           int64_t timeout_ns, bool test_stall, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,86 @@
+// moe_internal.h -- definitions shared by the host side (api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kRouteBlock = 128;   // tokens per router CTA (= rows of one router MMA tile)
+constexpr int kTileM = 128;        // rows per expert-GEMM m-tile
+constexpr int kGroupM = 8;         // m-tiles per scheduling group (weight-tile reuse in L2)
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 256;
+
+// Status word slots in the workspace header.
+enum : int { kHdrStatus = 0, kHdrWhere = 1, kHdrNumGroups = 2, kHdrNumMTiles = 3 };
+
+// Layer shape as the kernels see it.
+struct Shape {
+  int64_t T;
+  int64_t N;      // T * k routed rows
+  int d, E, k, F;
+  int nblk;       // router blocks of kRouteBlock tokens
+  float tau;
+  int has_bias;
+  int keep_logits;
+  int act_bf16;   // x and weights are bf16 (else fp32)
+  int out_bf16;   // y is bf16 (else fp32)
+  int max_groups; // capacity of the group table
+};
+
+// Device pointers into one workspace.
+struct Ws {
+  uint32_t* hdr;        // [64] status word, failure site, scheduler totals
+  float* aux;           // scalar
+  int32_t* blk_cnt;     // [nblk, E] rows per (router block, expert)
+  float* blk_psum;      // [nblk, E] sum over the block's tokens of p[t,e]
+  int32_t* local_rank;  // [N] rank of slot (t,j) among its block's slots with the same expert
+  int32_t* topk_idx;    // [N]
+  float* topk_gate;     // [N]
+  int32_t* counts;      // [E]
+  int32_t* offsets;     // [E+1]
+  int32_t* blk_base;    // [nblk, E] first row of (block, expert) in dispatch order
+  int32_t* grp_expert;  // [max_groups] expert of scheduling group g
+  int32_t* grp_mtile0;  // [max_groups] first m-tile (within the expert) of group g
+  int32_t* grp_mpre;    // [max_groups+1] prefix count of m-tiles over groups
+  int32_t* perm_src;    // [N]
+  int32_t* perm_slot;   // [N]
+  float* gate_perm;     // [N]
+  int32_t* slot_pos;    // [N]
+  float* logits;        // [T, E] or null
+  void* xp;             // [N, d]
+  void* h;              // [N, F]
+  void* yslot;          // [N, d]
+};
+
+// Fixed layout of one workspace: byte offsets of each region.
+struct WsLayout {
+  size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
+      grp_expert, grp_mtile0, grp_mpre, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
+      yslot, total;
+};
+
+WsLayout ws_layout(const Shape& s);
+Ws ws_bind(const Shape& s, void* base);
+
+struct Weights {
+  const void* x;
+  const void* wr;
+  const float* bias;
+  const void* w1;
+  const void* w3;
+  const void* w2;
+  void* y;
+};
+
+// Kernel launchers (each returns the launch's cudaError_t).
+cudaError_t launch_route_simt(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st);
+cudaError_t launch_scan(const Shape& s, const Ws& ws, cudaStream_t st);
+cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
+cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
+cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
+
+}  // namespace moe

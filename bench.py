@@ -1,0 +1,349 @@
+"""Benchmark of the sparse-MoE forward on GB300 (one JSON line on stdout, rank 0).
+
+Workload (default): the coarse-expert layer, T=4096 tokens, d_model=2048, E=8 experts, top-2,
+d_expert=8192, bf16 inputs, seeded synthetic data.  A step is one whole forward (router,
+scan, permute, grouped SwiGLU GEMM, grouped down-projection with gate and un-permute,
+combine, balancing scalar) through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on its own GPU
+(the forward has no exchange step on one device; "replicas only"), the timed region is
+bracketed by barriers, and the max time over ranks is used.
+
+--impl reference times the CPU oracle (the plain fp64 C implementation) on the host cores
+on a bounded sample of the same workload; it is the baseline the GPU path is compared to.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE fwd tokens/s and grouped-GEMM TFLOP/s (% of GB300 BF16 peak), 1 GPU"
+STAGES = ["route", "scan", "permute", "gemm1_swiglu", "gemm2_gate", "combine"]
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="coarse_e8")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling a smaller case)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(shape, world):
+    return {"workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
+            "d_expert": shape.F, "dtype": shape.dtype, "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sust=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_routing_grouped_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.ncu.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources") != kernel_source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "100"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), hw=parts[5], hwt=parts[6],
+                                     swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sms = sorted(r["sm"] for r in rows)
+        reasons = set()
+        for r in rows:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def cpu_baseline(shape, inputs, target_s):
+    """Time the oracle's whole forward on the first n tokens of the workload (a bounded
+    sample: about target_s seconds of CPU work).  Returns the cpu_baseline dict."""
+    import numpy as np
+    import oracle
+    host = inputs.numpy_for_oracle()
+
+    def run(n):
+        o = oracle.Oracle(n, shape.d, shape.E, shape.k, shape.F, tau=shape.tau, dtype=shape.dtype)
+        t0 = time.perf_counter()
+        o.forward(np.ascontiguousarray(host["x"][:n]), host["wr"], host["bias"], host["w1"], host["w3"], host["w2"])
+        return time.perf_counter() - t0
+
+    n0 = min(shape.T, 16)
+    t_small = run(n0)
+    n = int(min(shape.T, max(n0, n0 * target_s / max(t_small, 1e-6))))
+    t = run(n) if n != n0 else t_small
+    return {"value": n / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"whole forward of the first {n} of {shape.T} tokens of {shape.name} (fp64 C oracle, "
+                      f"OpenMP over tokens), {t:.1f} s wall"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle on the host cores, rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from top_routing_grouped_gb300.workloads import SHAPES, make_inputs
+    import oracle
+    shape = SHAPES[args.workload]
+    inputs = make_inputs(shape, seed=0)
+    # each step: a sample sized to ~per_step seconds, so the whole run stays within a few minutes
+    per_step = min(20.0, max(0.05, 60.0 / max(args.steps + args.warmup, 1)))
+    import numpy as np
+    host = inputs.numpy_for_oracle()
+
+    def run(n):
+        o = oracle.Oracle(n, shape.d, shape.E, shape.k, shape.F, tau=shape.tau, dtype=shape.dtype)
+        t0 = time.perf_counter()
+        o.forward(np.ascontiguousarray(host["x"][:n]), host["wr"], host["bias"], host["w1"], host["w3"], host["w2"])
+        return time.perf_counter() - t0
+
+    n0 = min(4, shape.T)
+    t0 = run(n0)
+    n = int(min(shape.T, max(1, n0 * per_step / max(t0, 1e-6))))
+    for _ in range(args.warmup):
+        run(n)
+    times = [run(n) for _ in range(args.steps)]
+    tot = sum(times)
+    value = n * len(times) / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(workload_config(shape, args.gpus), tokens_per_step=n),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"each step: whole forward of the first {n} of {shape.T} tokens"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from top_routing_grouped_gb300 import moe
+    from top_routing_grouped_gb300.workloads import SHAPES, make_inputs
+
+    shape = SHAPES[args.workload]
+    if args.tokens:
+        shape = shape.with_(T=args.tokens)
+    inputs = make_inputs(shape, seed=0)
+    dev = inputs.to("cuda")
+    plan = moe.MoEPlan.for_shape(shape)
+    assert plan.stage_names == STAGES
+    ws = plan.new_workspace()
+    y = torch.empty(shape.T, shape.d, dtype=plan.out_dtype, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    targs = (dev.x, dev.w_router, dev.bias, dev.w1, dev.w3, dev.w2, y, ws)
+
+    for _ in range(args.warmup):
+        plan.forward(*targs)
+    st = plan.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(K):
+            flush.zero_()  # L2 flush between steps, outside the events
+            for s in range(len(STAGES)):
+                ev[i][s].record(stream)
+                plan.forward_stage(s, *targs)
+            ev[i][len(STAGES)].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = plan.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+    stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(K)) / K for s in range(len(STAGES))]
+    step_ms = sum(ev[i][0].elapsed_time(ev[i][len(STAGES)]) for i in range(K)) / K
+    t_total = torch.tensor([step_ms * K], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t_total, op=dist.ReduceOp.MAX)
+    max_ms = float(t_total.item())
+    tokens = shape.T * K * world
+    value = tokens / (max_ms / 1e3)
+
+    # end to end through the host-buffer entry point: pinned x in, pinned y out, every step
+    e2e = None
+    if not args.no_e2e:
+        x_host = inputs.x.pin_memory()
+        y_host = torch.empty(shape.T, shape.d, dtype=plan.out_dtype).pin_memory()
+        x_dev = torch.empty_like(dev.x)
+        hargs = (x_host, x_dev, dev.w_router, dev.bias, dev.w1, dev.w3, dev.w2, y, y_host, ws)
+        for _ in range(3):
+            plan.forward_host(*hargs)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            plan.forward_host(*hargs)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        assert torch.equal(y_host.to("cuda"), y), "host-buffer forward disagrees with the device forward"
+        e2e = {"value": shape.T * K * world / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+               "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}
+
+    if rank == 0:
+        pk = peaks()
+        gemm_flops = shape.expert_flops
+        g1_ms, g2_ms = stage_ms[3], stage_ms[4]
+        g1_flops = 4 * shape.N * shape.d * shape.F  # the dominant kernel: SwiGLU GEMM (W1 and W3)
+        g1_tflops = g1_flops / (g1_ms / 1e3) / 1e12
+        gemm_tflops = gemm_flops / ((g1_ms + g2_ms) / 1e3) / 1e12
+        traffic = recorded_traffic(shape.name, "gemm1_swiglu")
+        x_bytes = shape.T * shape.d * 2
+        perm_bytes = x_bytes + shape.N * shape.d * 2 + 16 * shape.N
+        comb_bytes = shape.N * shape.d * 2 + shape.T * shape.d * 2
+        line = {
+            "metric": METRIC,
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded Gaussian, fan-in scaled)",
+            "config": workload_config(shape, world),
+            "grouped_gemm_tflops": gemm_tflops,
+            "grouped_gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16"],
+            "stage_ms": dict(zip(STAGES, stage_ms)),
+            "mover_gbs": {"permute": perm_bytes / (stage_ms[2] / 1e3) / 1e9,
+                          "combine": comb_bytes / (stage_ms[5] / 1e3) / 1e9},
+            "roofline": {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": g1_tflops, "peak": pk["bf16"],
+                         "unit": "TFLOP/s", "frac": g1_tflops / pk["bf16"], "traffic": traffic,
+                         "peak_source": f"{pk['src']} bf16 burst", "frac_of_sustained": g1_tflops / pk["bf16_sust"],
+                         "algorithmic": f"4*N*d*F = {g1_flops} FLOP per launch (N = T*k = {shape.N} rows)"},
+            "e2e": e2e,
+            "gpu_launches": len(STAGES) * K,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(shape, inputs, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -4,8 +4,8 @@
 
 namespace moe {
 
-// False until the tcgen05 kernels are in place; the plan then routes bf16 layers there.
-constexpr bool kTensorCorePathBuilt = false;
+// bf16 layers on MOE_PATH_AUTO run the tcgen05 kernels.
+constexpr bool kTensorCorePathBuilt = true;
 
 cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st);
 // mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yslot[slot] = gate * (H W2^T)

@@ -149,6 +149,34 @@ moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* view
  * if the synchronisation itself failed.  Each moe_forward clears the word first. */
 moe_status moe_get_device_status(moe_plan_t plan, const void* workspace, void* stream);
 
+/* Size in bytes of the static device buffer moe_route_noalloc() works in. */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Routing for callers that cannot allocate device memory.  The paper has no counterpart:
+ * this is a service of this library.  Some callers cannot call cudaMalloc at all (their
+ * memory budget is fixed in advance, or another runtime owns every device allocation, or
+ * the step must not risk an allocation failure part-way), so they cannot provide the
+ * workspace moe_forward needs.  This call runs only the router part of the forward --
+ * logits, softmax, top-k, gates, per-expert counts and the balancing scalar -- and keeps
+ * all of its scratch in one static device array of MOE_NOALLOC_SCRATCH_BYTES that the
+ * library holds on every GPU that loads it until the process exits.  Neither the caller
+ * nor the library allocates anything; the caller passes only inputs and outputs.
+ *   x, w_router, router_bias: as for moe_forward (router_bias may be NULL only when the
+ *     plan has no bias).
+ *   topk_idx [T,k] int32, topk_gate [T,k] fp32, expert_counts [E] int32, aux (one fp32):
+ *     device outputs, the same values moe_forward leaves in its workspace for this plan,
+ *     up to the rounding differences between its router kernels (the logits here are fp32
+ *     FMA sums).
+ * Returns MOE_ERR_UNSUPPORTED, with the sizes in moe_last_error(), when the plan needs more
+ * scratch than MOE_NOALLOC_SCRATCH_BYTES (256 + 4*T*k + 8*ceil(T/128)*E bytes, each part
+ * rounded up to 256).  The first call on each device looks up the array's device address
+ * with that device current; make that first call before any stream capture.  All calls
+ * share the one array and leave their contents in it: calls whose work overlaps on the
+ * GPU (other streams, other host threads) race and must be serialised by the caller.
+ * Asynchronous on `stream`. */
+moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
+                             int32_t* topk_idx, float* topk_gate, int32_t* expert_counts, float* aux, void* stream);
+
 /* Text of a status code, and a description of the last error on this thread. */
 const char* moe_status_string(moe_status s);
 const char* moe_last_error(void);

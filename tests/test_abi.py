@@ -18,6 +18,7 @@ def declared_functions():
         text = open(os.path.join(HEADER_DIR, fn)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"^\s*#[^\n]*", "", text, flags=re.M)   # preprocessor lines
         for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(([^;{]*)\)\s*;", text):
             if not m.group(1).startswith(("typedef",)) and m.group(1) not in ("sizeof",):
                 names.add(m.group(1))

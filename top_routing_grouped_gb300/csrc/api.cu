@@ -133,6 +133,13 @@ Ws ws_bind(const Shape& s, void* base) {
   return w;
 }
 
+const Shape* plan_shape(moe_plan_t plan) { return &plan->shape; }
+
+moe_status set_last_error(moe_status st, const char* msg) {
+  g_last_error = msg;
+  return st;
+}
+
 }  // namespace moe
 
 extern "C" {

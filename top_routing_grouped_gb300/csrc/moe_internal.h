@@ -83,4 +83,8 @@ cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, in
 cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
 
+// Plan internals for entry points defined outside api.cu.
+const Shape* plan_shape(moe_plan_t plan);
+moe_status set_last_error(moe_status st, const char* msg);
+
 }  // namespace moe

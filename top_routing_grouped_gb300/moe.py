@@ -60,6 +60,8 @@ _lib.moe_get_device_status.argtypes = [_P, _P, _P]
 _lib.moe_get_device_status.restype = ctypes.c_int
 _lib.moe_status_string.argtypes = [ctypes.c_int]
 _lib.moe_status_string.restype = ctypes.c_char_p
+_lib.moe_route_noalloc.argtypes = [_P] * 8 + [_P]
+_lib.moe_route_noalloc.restype = ctypes.c_int
 _lib.moe_last_error.argtypes = []
 _lib.moe_last_error.restype = ctypes.c_char_p
 
@@ -153,6 +155,13 @@ class MoEPlan:
             out = torch.empty((), dtype=torch.float32, device=workspace.device)
         _check(_lib.moe_aux_loss(self._h, _ptr(workspace), _ptr(out), _stream(stream)), "moe_aux_loss")
         return out
+
+    def route_noalloc(self, x, w_router, bias, topk_idx, topk_gate, expert_counts, aux, stream=None):
+        """Routing only, with the library's static scratch (moe_route_noalloc): for callers
+        that cannot allocate device memory.  All outputs are caller-provided tensors."""
+        _check(_lib.moe_route_noalloc(self._h, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
+                                      _ptr(topk_gate), _ptr(expert_counts), _ptr(aux), _stream(stream)),
+               "moe_route_noalloc")
 
     def device_status(self, workspace, stream=None):
         """Synchronises the stream; returns the status code (MOE_OK == 0)."""

@@ -63,13 +63,19 @@ def peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
 
 
-def kernel_source_digest():
+# sources each profiled kernel is built from: a recorded ncu traffic figure is only used
+# while these files are unchanged
+KERNEL_SOURCES = {
+    "gemm1_swiglu": ["gemm_tc.cu", "gemm_tc.h", "tc_ptx.cuh", "device_common.cuh", "moe_internal.h"],
+}
+
+
+def kernel_source_digest(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_routing_grouped_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+    for fn in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -84,7 +90,7 @@ def recorded_traffic(workload, kernel):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources") != kernel_source_digest():
+    if vals.get("kernel_sources") != kernel_source_digest(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])

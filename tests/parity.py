@@ -2,9 +2,11 @@
 
 Comparison rules (tolerances derived in the design notes):
   * logits:   |z_gpu - z| <= 1e-5 (1 + |z|)
-  * routing:  bit-exact indices for every *clear* token, i.e. one whose fp32 logits have
-              z_(k) - z_(k+1) > 1e-4 (k = E: every token is clear); a token that is not
-              clear is checked against the oracle run with the GPU's own choice;
+  * routing:  for every *clear* token, i.e. one whose fp32 logits have
+              z_(k) - z_(k+1) > 1e-4 (k = E: every token is clear), the chosen expert set is
+              bit-exact and the slot order descends in the oracle's logits up to 1e-4 (two
+              chosen experts closer than that may swap slots); every other token is checked
+              against the oracle run with the GPU's own choice;
   * gates:    |g_gpu - g| <= 1e-4 (g + 1e-12)   (g = oracle softmax at the GPU's indices)
   * dispatch: counts, offsets, perm_src, perm_slot bit-exact against the oracle's
               dispatch of the GPU's indices; Xp = x[perm_src] bit-exact (a copy);
@@ -81,15 +83,17 @@ def check_routing(orc, host, bias, got, rep):
         assert err.max() <= LOGIT_RTOL, f"logits off by {err.max()}"
     clear = clear_tokens(z, k)
     rep.add("clear tokens", f"{int(clear.sum())}/{T}")
-    # indices: exact on clear tokens against the oracle's own top-k
+    # indices: on clear tokens the chosen set is exactly the oracle's; the order inside it
+    # follows the oracle's logits wherever neighbours differ by more than the margin (two
+    # chosen experts within the margin of each other may come in either order)
     zs32 = z.astype(np.float32)
-    bad = np.where(clear & np.any(gidx != oidx, axis=1))[0]
-    assert bad.size == 0, f"{bad.size} clear tokens routed differently, e.g. token {bad[:5]}"
-    # every token: k distinct valid experts, descending in the oracle's logits up to the margin
+    bad = np.where(clear & np.any(np.sort(gidx, axis=1) != np.sort(oidx, axis=1), axis=1))[0]
+    assert bad.size == 0, f"{bad.size} clear tokens chose a different expert set, e.g. token {bad[:5]}"
     assert gidx.min() >= 0 and gidx.max() < E
-    assert all(len(set(r)) == k for r in gidx[~clear].tolist())
+    assert all(len(set(r)) == k for r in gidx.tolist())
     gz = np.take_along_axis(zs32, gidx, axis=1).astype(np.float64)
-    assert np.all(gz[:, :-1] - gz[:, 1:] >= -MARGIN)
+    assert np.all(gz[:, :-1] - gz[:, 1:] >= -MARGIN), "chosen experts not in descending logit order"
+    rep.add("slots in oracle order", f"{int(np.all(gidx == oidx, axis=1).sum())}/{T}")
     # gates: the oracle's softmax at the GPU's indices
     gref = np.take_along_axis(p, gidx, axis=1)
     gerr = np.abs(ggate - gref) / (gref + GATE_FLOOR)

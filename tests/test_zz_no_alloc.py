@@ -5,8 +5,9 @@ that must not fail half-way on an allocation) cannot hand moe_forward a workspac
 no-alloc entry point keeps its scratch in a static device array inside the library.  This
 test calls it through the C ABI twice in a row (the second call reuses the array the first
 one left behind) and checks both results against the routing that moe_forward leaves in its
-workspace, under the same rules as the parity tests: indices bit-exact on every token whose
-logit margin exceeds 1e-4, gates within 1e-4, counts exact (or, if a token is not clear,
+workspace, under the same rules as the parity tests: the chosen expert set bit-exact on
+every token whose logit margin exceeds 1e-4 (slots may swap only between experts within that
+margin of each other), gates within 1e-4, counts exact (or, if a token is not clear,
 consistent with the returned indices), aux within 1e-5 relative.
 
 This file is named to be collected last, so that a run stopping at its first failure has
@@ -52,7 +53,8 @@ def test_route_noalloc_matches_forward_twice(shape):
     ref_gate = v["topk_gate"].cpu().numpy().astype(np.float64)
     ref_counts = v["expert_counts"].cpu().numpy()
     ref_aux = float(v["aux"].item())
-    clear = clear_tokens(v["logits"].cpu().numpy(), shape.k)
+    logits = v["logits"].cpu().numpy()
+    clear = clear_tokens(logits, shape.k)
 
     lib = moe.lib()
     stream = torch.cuda.current_stream()
@@ -70,8 +72,13 @@ def test_route_noalloc_matches_forward_twice(shape):
         gg = gate.cpu().numpy().astype(np.float64)
         gc = counts.cpu().numpy()
         ga = float(aux.item())
-        np.testing.assert_array_equal(gi[clear], ref_idx[clear], err_msg=f"call {call}: indices")
+        # same expert set on every clear token; inside it, slots may swap only between
+        # experts whose logits lie within the 1e-4 margin of each other
+        np.testing.assert_array_equal(np.sort(gi[clear], axis=1), np.sort(ref_idx[clear], axis=1),
+                                      err_msg=f"call {call}: expert sets")
         assert gi.min() >= 0 and gi.max() < shape.E
+        zl = np.take_along_axis(logits.astype(np.float32), gi, axis=1).astype(np.float64)
+        assert np.all(zl[:, :-1] - zl[:, 1:] >= -1e-4), f"call {call}: slots out of logit order"
         same = np.all(gi == ref_idx, axis=1)
         gerr = np.abs(gg[same] - ref_gate[same]) / (ref_gate[same] + 1e-12)
         assert gerr.max() <= 1e-4, f"call {call}: gates off by {gerr.max()}"

@@ -312,7 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -326,7 +328,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 row-major [rows, cols] tensor, boxes of [box_rows, 64] with 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cols, rows};
@@ -339,33 +341,27 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-}  // namespace
-
 cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
                            int64_t timeout_ns, bool test_stall, cudaStream_t st) {
   CUtensorMap mA, mB, mB3;
   cudaError_t e;
   if (mode == 1) {
-    if ((e = make_map(&mA, ws.xp, (uint64_t)s.N, (uint64_t)s.d, kMmaM)) != cudaSuccess) return e;
-    if ((e = make_map(&mB, w.w1, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
-    if ((e = make_map(&mB3, w.w3, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mA, ws.xp, (uint64_t)s.N, (uint64_t)s.d, kMmaM)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mB, w.w1, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mB3, w.w3, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
         cudaSuccess)
       return e;
     gemm_tc_kernel<1><<<num_sms, kThreads, kSmemBytes, st>>>(mA, mB, mB3, s, ws, timeout_ns, test_stall ? 1 : 0);
   } else {
-    if ((e = make_map(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kMmaM)) != cudaSuccess) return e;
-    if ((e = make_map(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kMmaM)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(gemm_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
         cudaSuccess)
       return e;
     gemm_tc_kernel<2><<<num_sms, kThreads, kSmemBytes, st>>>(mA, mB, mB, s, ws, timeout_ns, test_stall ? 1 : 0);
   }
   return cudaGetLastError();
-}
-
-cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st) {
-  return launch_route_simt(s, ws, w, st);
 }
 
 }  // namespace moe

@@ -7,7 +7,13 @@ namespace moe {
 // bf16 layers on MOE_PATH_AUTO run the tcgen05 kernels.
 constexpr bool kTensorCorePathBuilt = true;
 
-cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st);
+#include <cuda.h>
+
+// Tensor map of a row-major bf16 [rows, cols] matrix, boxes of [box_rows, 64] elements with
+// 128-byte swizzling (the K-major operand layout of the tcgen05 kernels).
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int64_t timeout_ns, cudaStream_t st);
 // mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yslot[slot] = gate * (H W2^T)
 cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
                            int64_t timeout_ns, bool test_stall, cudaStream_t st);

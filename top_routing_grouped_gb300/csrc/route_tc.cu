@@ -1,0 +1,255 @@
+// route_tc.cu -- the router on the tensor cores: logits of 128 tokens x E experts per CTA
+// with tcgen05.mma (x tile [128 x 64] and W_r tile [E_pad x 64] per stage, TMA-fed, fp32
+// accumulators in TMEM), then the shared softmax / top-k / per-block counting epilogue.
+//
+// After "Distributed Training Part 4 ... MoE + Expert Parallelism" (jesamkim ai-tech-blog),
+// §3 Structure: the router is a linear layer followed by a softmax over the experts.  The
+// layer streams x once (2 bytes per element against 2E flops), so it is bound by HBM, not by
+// the MMA; the tensor cores only keep the E dot products per token off the SIMT pipes.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
+// warps 2..5 epilogue (warp w reads TMEM lanes 32*(w%4)..: rows of its 32 tokens).
+// Waits are bounded as in the expert GEMMs; if one runs out the block still finishes its
+// epilogue on zero logits (valid routing, status MOE_ERR_TIMEOUT) so no barrier is left open.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_tc.h"
+#include "route_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kXBytes = kRouteBlock * kBK * 2;  // 16 KB
+
+struct RouteCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int vote[4];
+};
+
+struct RouteGeom {
+  int e_pad;        // MMA N: E rounded up to a multiple of 16 (>= 16)
+  int n_acc;        // TMEM accumulators the K loop is spread over (summed in fp32 at the end)
+  int stages;
+  int stage_bytes;  // x tile + W_r tile
+  int body_bytes;   // max(stages * stage_bytes, logits + masks)
+  uint32_t tmem_cols;
+  size_t smem;      // dynamic shared memory
+};
+
+RouteGeom route_geom(const Shape& s) {
+  RouteGeom g;
+  g.e_pad = ((s.E + 15) / 16) * 16;
+  if (g.e_pad < 16) g.e_pad = 16;
+  g.stage_bytes = kXBytes + g.e_pad * kBK * 2;
+  // up to ~96 KB of ring so that two CTAs share an SM (more bytes in flight per SM)
+  g.stages = (96 * 1024) / g.stage_bytes;
+  if (g.stages > kMaxStages) g.stages = kMaxStages;
+  if (g.stages < 2) g.stages = 2;
+  const int zs = kRouteBlock * (s.E + 1) * 4 + 4 * s.E * 4;
+  g.body_bytes = g.stages * g.stage_bytes > zs ? g.stages * g.stage_bytes : zs;
+  g.body_bytes = (g.body_bytes + 1023) / 1024 * 1024;
+  // The tensor core's fp32 accumulation chain over K = d loses more than a SIMT sum; K-block
+  // kb goes to accumulator kb % n_acc and the epilogue adds the n_acc partial sums in fp32
+  // (round to nearest), which keeps the logits within a few 1e-7 relative.
+  g.n_acc = 512 / g.e_pad;
+  if (g.n_acc > 4) g.n_acc = 4;
+  uint32_t c = 32;
+  while (c < (uint32_t)(g.e_pad * g.n_acc)) c <<= 1;
+  g.tmem_cols = c;
+  // more than half of TMEM: make the CTA big enough in shared memory that two never share an
+  // SM (the second would only wait in tcgen05.alloc)
+  if (g.tmem_cols > 256 && g.body_bytes < 120 * 1024) g.body_bytes = 120 * 1024;
+  g.smem = 1024 + (size_t)g.body_bytes + sizeof(RouteCtl);
+  return g;
+}
+
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                             const __grid_constant__ CUtensorMap tmW, Shape s, Ws ws,
+                                                             Weights w, RouteGeom g, int64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* body = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  RouteCtl* ctl = reinterpret_cast<RouteCtl*>(body + g.body_bytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int blk = blockIdx.x;
+  const int kblocks = s.d / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < g.stages; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->empty[i]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&ctl->tfull), 1);
+    ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), g.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort;
+  uint32_t issued = 0, issued_phase = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmX);
+      ptx::tma_prefetch_desc(&tmW);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
+          *abort_flag = 1;
+          record_error(ws, MOE_ERR_TIMEOUT, 0x600u);
+          break;
+        }
+        const uint32_t bar = ptx::smem_u32(&ctl->full[stage]);
+        const uint32_t sa = ptx::smem_u32(body + (size_t)stage * g.stage_bytes);
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)g.stage_bytes);
+        ptx::tma_load_2d(sa, &tmX, kb * kBK, blk * kRouteBlock, bar);
+        ptx::tma_load_2d(sa + kXBytes, &tmW, kb * kBK, 0, bar);
+        issued |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == g.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(kRouteBlock, g.e_pad);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&ctl->full[stage]), phase, timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t sa = ptx::smem_u32(body + (size_t)stage * g.stage_bytes);
+        const uint32_t sb = sa + kXBytes;
+        const uint32_t d_tmem = tmem + (uint32_t)((kb % g.n_acc) * g.e_pad);
+#pragma unroll
+        for (int ks = 0; ks < kBK / 16; ++ks)
+          ptx::mma_bf16(d_tmem, ptx::desc_kmajor_sw128(sa + ks * 32), ptx::desc_kmajor_sw128(sb + ks * 32), idesc,
+                        (kb >= g.n_acc || ks != 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&ctl->empty[stage]));
+        if (++stage == g.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) {
+        ptx::mma_commit(ptx::smem_u32(&ctl->tfull));
+      } else {
+        *abort_flag = 1;
+        record_error(ws, MOE_ERR_TIMEOUT, 0x610u);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // token row of this block
+    bool ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull), 0u, timeout_ns, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) ctl->vote[q] = ok ? 1 : 0;
+    named_barrier(2, kRouteBlock);
+    const bool all_ok = ctl->vote[0] && ctl->vote[1] && ctl->vote[2] && ctl->vote[3];
+    float* z_s = reinterpret_cast<float*>(body);
+    uint32_t* mask_s = reinterpret_cast<uint32_t*>(z_s + kRouteBlock * (s.E + 1));
+    const int ldz = s.E + 1;
+    if (all_ok) {
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+      const int used = kblocks < g.n_acc ? kblocks : g.n_acc;  // accumulators that were written
+      for (int c = 0; c < g.e_pad; c += 16) {
+        float sum[16];
+        for (int a = 0; a < used; ++a) {
+          uint32_t v[16];
+          tmem_ld_16cols(t_row + (uint32_t)(a * g.e_pad + c), v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum[i] = a == 0 ? __uint_as_float(v[i]) : sum[i] + __uint_as_float(v[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = c + i;
+          if (e < s.E) {
+            float z = sum[i];
+            if (s.has_bias) z += w.bias[e];
+            z_s[r * ldz + e] = z / s.tau;
+          }
+        }
+      }
+    } else {
+      if (lane == 0 && q == 0) record_error(ws, MOE_ERR_TIMEOUT, 0x620u);
+      for (int e = 0; e < s.E; ++e) z_s[r * ldz + e] = 0.f;
+    }
+    route_finish(s, ws, blk, r, z_s, ldz, mask_s, /*bar_id=*/1);
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0)
+      for (int st = 0; st < g.stages; ++st)
+        if (issued & (1u << st))
+          ptx::mbar_wait(ptx::smem_u32(&ctl->full[st]), (issued_phase >> st) & 1u, timeout_ns, nullptr);
+    if (warp == 1 && lane == 0) {
+      ptx::mma_commit(ptx::smem_u32(&ctl->drain));
+      ptx::mbar_wait(ptx::smem_u32(&ctl->drain), 0u, timeout_ns, nullptr);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, g.tmem_cols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int64_t timeout_ns, cudaStream_t st) {
+  const RouteGeom g = route_geom(s);
+  CUtensorMap mx, mw;
+  cudaError_t e;
+  if ((e = make_tmap_bf16(&mx, w.x, (uint64_t)s.T, (uint64_t)s.d, kRouteBlock)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16(&mw, w.wr, (uint64_t)s.E, (uint64_t)s.d, (uint32_t)g.e_pad)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem)) !=
+      cudaSuccess)
+    return e;
+  route_tc_kernel<<<s.nblk, kThreads, g.smem, st>>>(mx, mw, s, ws, w, g, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -46,6 +46,21 @@ def parse():
     return ap.parse_args()
 
 
+def reduce_max(value, device):
+    """Max of a per-rank float over all ranks (the rank's own value when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(units_per_rank_step, steps, world, max_ms):
+    """Whole-job rate: the units every rank processed, over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (max_ms / 1e3)
+
+
 def workload_config(shape, world):
     return {"workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
             "d_expert": shape.F, "dtype": shape.dtype, "parallelism": "replicas" if world > 1 else "single GPU",
@@ -282,12 +297,8 @@ def main():
         raise RuntimeError(f"device status {st} after the timed region")
     stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(K)) / K for s in range(len(STAGES))]
     step_ms = sum(ev[i][0].elapsed_time(ev[i][len(STAGES)]) for i in range(K)) / K
-    t_total = torch.tensor([step_ms * K], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_total, op=dist.ReduceOp.MAX)
-    max_ms = float(t_total.item())
-    tokens = shape.T * K * world
-    value = tokens / (max_ms / 1e3)
+    max_ms = reduce_max(step_ms * K, "cuda")
+    value = throughput(shape.T, K, world, max_ms)
 
     # end to end through the host-buffer entry point: pinned x in, pinned y out, every step
     e2e = None
@@ -305,11 +316,9 @@ def main():
             plan.forward_host(*hargs)
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        e_ms = reduce_max(e0.elapsed_time(e1), "cuda")
         assert torch.equal(y_host.to("cuda"), y), "host-buffer forward disagrees with the device forward"
-        e2e = {"value": shape.T * K * world / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
+        e2e = {"value": throughput(shape.T, K, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}
 

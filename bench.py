@@ -81,7 +81,7 @@ def peaks():
 # sources each profiled kernel is built from: a recorded ncu traffic figure is only used
 # while these files are unchanged
 KERNEL_SOURCES = {
-    "gemm1_swiglu": ["gemm_tc.cu", "gemm_tc.h", "tc_ptx.cuh", "device_common.cuh", "moe_internal.h"],
+    "gemm1_swiglu": ["gemm_tc2.cu", "gemm_tc.h", "tc_ptx.cuh", "device_common.cuh", "moe_internal.h"],
 }
 
 

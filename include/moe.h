@@ -56,9 +56,11 @@ typedef enum {
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
 /* Which kernels run the router and the expert GEMMs.
- *   MOE_PATH_AUTO: bf16 -> tcgen05/TMEM/TMA kernels; fp32 -> fp32 SIMT kernels (true fp32).
- *   MOE_PATH_SIMT: SIMT kernels for every dtype (fp32 FMA, a cross-check of the tensor path). */
-typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_SIMT = 1 } moe_path;
+ *   MOE_PATH_AUTO:   bf16 -> tcgen05/TMEM/TMA kernels, expert GEMMs on CTA pairs (2-SM MMA);
+ *                    fp32 -> fp32 SIMT kernels (true fp32).
+ *   MOE_PATH_SIMT:   SIMT kernels for every dtype (fp32 FMA, a cross-check of the tensor path).
+ *   MOE_PATH_TC_1SM: bf16 only: as AUTO but the expert GEMMs run one CTA per tile (1-SM MMA). */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_SIMT = 1, MOE_PATH_TC_1SM = 2 } moe_path;
 
 /* flags */
 #define MOE_FLAG_KEEP_LOGITS 1u /* the router also stores its fp32 logits z [T,E] in the workspace */

@@ -13,7 +13,7 @@ from top_routing_grouped_gb300.workloads import SHAPES, ORDER, MoEShape, make_in
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["auto", "simt"]
+PATHS = ["auto", "tc1", "simt"]
 
 
 @pytest.fixture(scope="module")
@@ -125,7 +125,7 @@ def smallest_expert_tokens(got, cap=48):
 
 
 @pytest.mark.parametrize("name", ORDER[1:])
-@pytest.mark.parametrize("path", ["auto"])
+@pytest.mark.parametrize("path", ["auto", "tc1"])
 def test_full_size_workloads(moe, name, path):
     """The listed workloads at full size: every token's routing and dispatch, sampled H
     rows and y tokens."""

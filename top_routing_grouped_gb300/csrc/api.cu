@@ -16,7 +16,8 @@ struct moe_plan_s {
   moe_config cfg;
   moe::Shape shape;
   moe::WsLayout layout;
-  bool tc;          // tensor-core router and expert GEMMs (bf16 layers on MOE_PATH_AUTO)
+  bool tc;          // tensor-core router and expert GEMMs (bf16 layers, not MOE_PATH_SIMT)
+  bool pair;        // expert GEMMs on CTA pairs (MOE_PATH_AUTO)
   int device = -1;  // device the cached attributes belong to
   int num_sms = 0;
   int64_t timeout_ns;
@@ -93,6 +94,7 @@ WsLayout ws_layout(const Shape& s) {
   L.grp_expert = take((size_t)s.max_groups * 4);
   L.grp_mtile0 = take((size_t)s.max_groups * 4);
   L.grp_mpre = take(((size_t)s.max_groups + 1) * 4);
+  L.grp_ppre = take(((size_t)s.max_groups + 1) * 4);
   L.perm_src = take(N * 4);
   L.perm_slot = take(N * 4);
   L.gate_perm = take(N * 4);
@@ -122,6 +124,7 @@ Ws ws_bind(const Shape& s, void* base) {
   w.grp_expert = reinterpret_cast<int32_t*>(b + L.grp_expert);
   w.grp_mtile0 = reinterpret_cast<int32_t*>(b + L.grp_mtile0);
   w.grp_mpre = reinterpret_cast<int32_t*>(b + L.grp_mpre);
+  w.grp_ppre = reinterpret_cast<int32_t*>(b + L.grp_ppre);
   w.perm_src = reinterpret_cast<int32_t*>(b + L.perm_src);
   w.perm_slot = reinterpret_cast<int32_t*>(b + L.perm_slot);
   w.gate_perm = reinterpret_cast<float*>(b + L.gate_perm);
@@ -172,13 +175,15 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
   if (!(c.router_temperature > 0.f) || !isfinite(c.router_temperature))
     return fail(MOE_ERR_INVALID_ARG, "router_temperature must be finite and > 0");
   if (c.has_router_bias != 0 && c.has_router_bias != 1) return fail(MOE_ERR_INVALID_ARG, "has_router_bias must be 0 or 1");
-  if (c.path != MOE_PATH_AUTO && c.path != MOE_PATH_SIMT) return fail(MOE_ERR_INVALID_ARG, "bad path");
+  if (c.path != MOE_PATH_AUTO && c.path != MOE_PATH_SIMT && c.path != MOE_PATH_TC_1SM)
+    return fail(MOE_ERR_INVALID_ARG, "bad path");
   if (c.flags & ~(MOE_FLAG_KEEP_LOGITS | MOE_FLAG_TEST_STALL)) return fail(MOE_ERR_INVALID_ARG, "unknown flags");
   const int64_t N = c.T * (int64_t)c.top_k;
   if (N > (int64_t)INT32_MAX / 2 || N * (int64_t)(c.d_model > c.d_expert ? c.d_model : c.d_expert) > ((int64_t)1 << 40))
     return fail(MOE_ERR_UNSUPPORTED, "T * top_k (or the routed activations) too large");
   const bool bf16 = c.act_dtype == MOE_BF16;
-  const bool tc = bf16 && c.path == MOE_PATH_AUTO && moe::kTensorCorePathBuilt;
+  if (c.path == MOE_PATH_TC_1SM && !bf16) return fail(MOE_ERR_INVALID_ARG, "MOE_PATH_TC_1SM needs bf16 inputs");
+  const bool tc = bf16 && c.path != MOE_PATH_SIMT && moe::kTensorCorePathBuilt;
   if (!bf16 && c.d_model % 4 != 0) return fail(MOE_ERR_UNSUPPORTED, "fp32 layers need d_model %% 4 == 0");
   if (bf16 && c.d_model % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "bf16 layers need d_model %% 8 == 0");
   if (tc && (c.d_model % 64 != 0 || c.d_expert % 64 != 0))
@@ -207,6 +212,7 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
   s.max_groups = (int)(N / ((int64_t)moe::kTileM * moe::kGroupM) + 2 * (int64_t)c.n_experts + 2);
   p->layout = moe::ws_layout(s);
   p->tc = tc;
+  p->pair = tc && c.path == MOE_PATH_AUTO;
   p->timeout_ns = c.wait_timeout_ns > 0 ? c.wait_timeout_ns : 2000000000LL;
   *plan = p;
   *workspace_bytes = p->layout.total;
@@ -254,14 +260,17 @@ static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& 
     case 1: e = moe::launch_scan(s, ws, st); break;
     case 2: e = moe::launch_permute(s, ws, w, plan->num_sms, st); break;
     case 3:
-      e = plan->tc ? moe::launch_gemm_tc(1, s, ws, w, plan->num_sms, plan->timeout_ns,
-                                         (plan->cfg.flags & MOE_FLAG_TEST_STALL) != 0, st)
-                   : moe::launch_gemm1_simt(s, ws, w, plan->num_sms, st);
+    case 4: {
+      const int mode = stage == 3 ? 1 : 2;
+      const bool stall = mode == 1 && (plan->cfg.flags & MOE_FLAG_TEST_STALL) != 0;
+      if (plan->pair)
+        e = moe::launch_gemm_tc_pair(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, st);
+      else if (plan->tc)
+        e = moe::launch_gemm_tc(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, st);
+      else
+        e = mode == 1 ? moe::launch_gemm1_simt(s, ws, w, plan->num_sms, st) : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, st);
       break;
-    case 4:
-      e = plan->tc ? moe::launch_gemm_tc(2, s, ws, w, plan->num_sms, plan->timeout_ns, false, st)
-                   : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, st);
-      break;
+    }
     case 5: e = moe::launch_combine(s, ws, w, plan->num_sms, st); break;
     default: return fail(MOE_ERR_INVALID_ARG, "stage %d out of range", stage);
   }

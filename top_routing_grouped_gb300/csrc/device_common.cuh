@@ -63,4 +63,29 @@ __device__ __forceinline__ TileInfo decode_tile(const Ws& ws, int ngroups, int n
   return ti;
 }
 
+// Decode linear pair-tile id -> the m-tile of CTA `rank` (0/1) of a CTA pair.  A pair tile
+// is two consecutive m-tiles of one scheduling group (the second may not exist: rows <= 0)
+// times one n-tile; group g owns pair tiles [n_tiles * ppre[g], n_tiles * ppre[g+1]) and
+// inside a group the pair index runs fastest.
+__device__ __forceinline__ TileInfo decode_pair_tile(const Ws& ws, int ngroups, int n_tiles, int tile, int rank) {
+  const int q = tile / n_tiles;
+  int lo = 0, hi = ngroups - 1;  // largest g with ppre[g] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&ws.grp_ppre[mid]) <= q) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int p_begin = __ldg(&ws.grp_ppre[g]);
+  const int gp = __ldg(&ws.grp_ppre[g + 1]) - p_begin;
+  const int local = tile - n_tiles * p_begin;
+  TileInfo ti;
+  ti.e = __ldg(&ws.grp_expert[g]);
+  ti.n_idx = local / gp;
+  const int mt = __ldg(&ws.grp_mtile0[g]) + 2 * (local % gp) + rank;
+  ti.row0 = __ldg(&ws.offsets[ti.e]) + mt * kTileM;
+  const int rem = __ldg(&ws.counts[ti.e]) - mt * kTileM;
+  ti.rows = rem < kTileM ? rem : kTileM;  // <= 0: no such m-tile (odd group), nothing stored
+  return ti;
+}
+
 }  // namespace moe

@@ -13,6 +13,11 @@ constexpr bool kTensorCorePathBuilt = true;
 // 128-byte swizzling (the K-major operand layout of the tcgen05 kernels).
 cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
+// 2-SM version (CTA pairs, tcgen05.mma.cta_group::2): same arguments and results.
+constexpr int kPairAccBufs = 2;  // TMEM accumulators per pair CTA (x 256 columns): double-buffered
+cudaError_t launch_gemm_tc_pair(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
+                                int64_t timeout_ns, bool test_stall, cudaStream_t st);
+
 cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int64_t timeout_ns, cudaStream_t st);
 // mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yslot[slot] = gate * (H W2^T)
 cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,

@@ -1,0 +1,362 @@
+// gemm_tc2.cu -- the grouped expert GEMMs on CTA pairs (2-SM tcgen05.mma, cta_group::2).
+//
+// Same operation as gemm_tc.cu (after "Distributed Training Part 4 ... MoE + Expert
+// Parallelism", jesamkim ai-tech-blog, §3 Structure / output formula, §4 Combine):
+//   mode 1:  H[p, n]           = SiLU(Xp[p] . W1_e[n]) * (Xp[p] . W3_e[n])
+//   mode 2:  Yslot[slot(p), n] = gate(p) * (H[p] . W2_e[n])
+//
+// A cluster of two CTAs on two SMs computes a 256 x 256 tile with one MMA stream issued by
+// the first CTA (the leader): each CTA loads only its own 128 rows of A and its half of the
+// 256 B rows (mode 1: the leader the W1 tile, the peer the W3 tile; mode 2: one half each),
+// so an SM pulls 32 KB per 64-deep K step instead of 48 KB and the ring holds 6 stages.
+// Both CTAs' loads signal the leader's "full" barrier; the leader's commits free the stage in
+// both CTAs (multicast arrive) and hand each CTA its 128 accumulator rows in its own TMEM.
+// The epilogue is the one-SM kernel's, per CTA; its warps release the accumulator to the
+// leader with a cluster-scope arrive.
+//
+// Waits are bounded (MOE_ERR_TIMEOUT, no trap); an abort raises the flag in both CTAs; the
+// pair meets at cluster barriers before TMEM is released.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "gemm_tc.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kRowsPerCta = 128;
+constexpr int kMmaM = 256;  // both CTAs
+constexpr int kMmaN = 256;
+constexpr int kMmaK = 16;
+constexpr int kABytes = kRowsPerCta * kBK * 2;    // 16 KB
+constexpr int kBHalfBytes = (kMmaN / 2) * kBK * 2;  // 16 KB
+constexpr int kStageBytes = kABytes + kBHalfBytes;
+constexpr int kAccCols = kMmaN;
+constexpr int kThreads = 256;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 4;
+
+struct Ctl2 {
+  uint64_t full[kStages];   // leader's: both CTAs' bytes of a stage
+  uint64_t empty[kStages];  // each CTA: stage free again (leader's multicast commit)
+  uint64_t tfull[2];        // each CTA: accumulator ready (leader's multicast commit)
+  uint64_t tempty[2];       // leader's: both CTAs' epilogue warps done with the accumulator
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t peer_tmem_base;  // the peer's allocation, written by the peer
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl2);
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu(float a) { return a / (1.0f + __expf(-a)); }
+
+__device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
+  ctl->abort = 1;
+  ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&ctl->abort), rank ^ 1u), 1u);
+}
+
+template <int kMode, int kAccBufs>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB3, Shape s, Ws ws, int64_t timeout_ns, int stall) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl2* ctl = reinterpret_cast<Ctl2*>(stages + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = (int)ptx::cluster_id_x();
+  const int ncl = (int)ptx::cluster_count_x();
+
+  const int ncols = kMode == 1 ? s.F : s.d;
+  const int K = kMode == 1 ? s.d : s.F;
+  const int bn = kMode == 1 ? kMmaN / 2 : kMmaN;  // output columns per tile
+  const int n_tiles = (ncols + bn - 1) / bn;
+  const int kblocks = K / kBK;
+  const int ngroups = (int)ws.hdr[kHdrNumGroups];
+  int total = (int)ws.hdr[kHdrNumPairs] * n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->tfull[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->tempty[i]), 2 * kEpiWarps);
+    }
+    ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    ctl->peer_tmem_base = 0xFFFFFFFFu;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+    if (kMode == 1) ptx::tma_prefetch_desc(&tmB3);
+  }
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive or load
+  if (warp == 2) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&ctl->tmem_base), kAccBufs * kAccCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  if (threadIdx.x == 0) ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&ctl->peer_tmem_base), rank ^ 1u), tmem);
+  ptx::cluster_sync();
+  if (ctl->peer_tmem_base != tmem) {  // a pair's accumulators must sit at the same TMEM address
+    if (threadIdx.x == 0) record_error(ws, MOE_ERR_INTERNAL, 0x700u + kMode);
+    total = 0;
+  }
+  volatile int* abort_flag = &ctl->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true, first = true;
+      const CUtensorMap* bmap = (kMode == 1 && rank == 1) ? &tmB3 : &tmB;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        const TileInfo ti = decode_pair_tile(ws, ngroups, n_tiles, tile, (int)rank);
+        const int brow = kMode == 1 ? ti.e * s.F + ti.n_idx * bn : ti.e * s.d + ti.n_idx * bn + (int)rank * (kMmaN / 2);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!(stall && first && leader)) {  // the stall hook withholds one stage of the leader
+            const uint32_t full_local = ptx::smem_u32(&ctl->full[stage]);
+            if (leader) ptx::mbar_arrive_expect_tx(full_local, 2 * kStageBytes);
+            const uint32_t bar = ptx::mapa(full_local, 0);
+            const uint32_t sa = ptx::smem_u32(stages + (size_t)stage * kStageBytes);
+            ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, ti.row0, bar);
+            ptx::tma_load_2d_pair(sa + kABytes, bmap, kb * kBK, brow, bar);
+          }
+          first = false;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_error(ws, MOE_ERR_TIMEOUT, 0x540u + kMode);
+        raise_abort(ctl, rank);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer (leader only)
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kMmaM, kMmaN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&ctl->full[stage]), phase, timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(stages + (size_t)stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kBK / kMmaK; ++ks)
+            ptx::mma_bf16_pair(d_tmem, ptx::desc_kmajor_sw128(sa + ks * kMmaK * 2),
+                               ptx::desc_kmajor_sw128(sb + ks * kMmaK * 2), idesc, (kb | ks) != 0 ? 1u : 0u);
+          ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->tfull[acc]), 0x3);
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        record_error(ws, MOE_ERR_TIMEOUT, 0x550u + kMode);
+        raise_abort(ctl, rank);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = cid; tile < total; tile += ncl) {
+      const TileInfo ti = decode_pair_tile(ws, ngroups, n_tiles, tile, (int)rank);
+      ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull[acc]), acc_phase, timeout_ns, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
+      const bool valid = r < ti.rows;
+      const int64_t p = (int64_t)ti.row0 + r;
+      const int n0 = ti.n_idx * bn;
+      if (kMode == 1) {
+        __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(ws.h) + p * s.F + n0;
+#pragma unroll 1
+        for (int c = 0; c < kMmaN / 2; c += 32) {
+          uint32_t a[32], g[32];
+          ptx::tmem_ld_32cols(t_row + c, a);
+          ptx::tmem_ld_32cols(t_row + kMmaN / 2 + c, g);
+          ptx::tmem_ld_wait();
+          if (valid && n0 + c < s.F) {
+            uint4* dst = reinterpret_cast<uint4*>(hrow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int i = v * 8 + u * 2;
+                ow[u] = pack_bf16x2(silu(__uint_as_float(a[i])) * __uint_as_float(g[i]),
+                                    silu(__uint_as_float(a[i + 1])) * __uint_as_float(g[i + 1]));
+              }
+              dst[v] = o;
+            }
+          }
+        }
+      } else {
+        int64_t slot = -1;
+        float gate = 0.f;
+        if (valid) {
+          slot = ws.perm_slot[p];
+          gate = ws.gate_perm[p];
+          if (slot < 0 || slot >= s.N) {
+            record_error(ws, MOE_ERR_INTERNAL, 0x560u);
+            slot = -1;
+          }
+        }
+        __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(ws.yslot) + slot * s.d + n0;
+#pragma unroll 1
+        for (int c = 0; c < kMmaN; c += 32) {
+          uint32_t a[32];
+          ptx::tmem_ld_32cols(t_row + c, a);
+          ptx::tmem_ld_wait();
+          if (slot >= 0 && n0 + c < s.d) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int i = v * 8 + u * 2;
+                ow[u] = pack_bf16x2(gate * __uint_as_float(a[i]), gate * __uint_as_float(a[i + 1]));
+              }
+              dst[v] = o;
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&ctl->tempty[acc]), 0));
+      if (++acc == kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      record_error(ws, MOE_ERR_TIMEOUT, 0x570u + kMode);
+      raise_abort(ctl, rank);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (leader && warp == 1 && lane == 0) {
+    // every pair MMA of this pair has finished writing both CTAs' TMEM
+    ptx::mma_commit_pair(ptx::smem_u32(&ctl->drain));
+    ptx::mbar_wait(ptx::smem_u32(&ctl->drain), 0u, timeout_ns, nullptr);
+  }
+  __syncthreads();
+  ptx::cluster_sync();  // neither CTA issues loads or MMAs any more
+  if (*abort_flag && threadIdx.x == 0) {
+    // copies already in flight land within microseconds; give them 200 us before the
+    // shared memory they target goes away
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 200000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, kAccBufs * kAccCols);
+  }
+}
+
+template <int kMode, int kAccBufs>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const Shape& s, const Ws& ws,
+                        int num_sms, int64_t timeout_ns, bool stall, cudaStream_t st) {
+  auto kern = gemm_tc2_kernel<kMode, kAccBufs>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many pairs as can be resident at once (persistent loop over pair tiles)
+  cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0 &&
+      2 * clusters < (int)cfg.gridDim.x)
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, b3, s, ws, timeout_ns, stall ? 1 : 0);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc_pair(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
+                                int64_t timeout_ns, bool test_stall, cudaStream_t st) {
+  CUtensorMap mA, mB, mB3;
+  cudaError_t e;
+  if (mode == 1) {
+    if ((e = make_tmap_bf16(&mA, ws.xp, (uint64_t)s.N, (uint64_t)s.d, kRowsPerCta)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mB, w.w1, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mB3, w.w3, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
+    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, s, ws, num_sms, timeout_ns, test_stall, st);
+  }
+  if ((e = make_tmap_bf16(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kRowsPerCta)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN / 2)) != cudaSuccess) return e;
+  return launch_pair<2, kPairAccBufs>(mA, mB, mB, s, ws, num_sms, timeout_ns, false, st);
+}
+
+}  // namespace moe

@@ -14,7 +14,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 
 // Status word slots in the workspace header.
-enum : int { kHdrStatus = 0, kHdrWhere = 1, kHdrNumGroups = 2, kHdrNumMTiles = 3 };
+enum : int { kHdrStatus = 0, kHdrWhere = 1, kHdrNumGroups = 2, kHdrNumMTiles = 3, kHdrNumPairs = 4 };
 
 // Layer shape as the kernels see it.
 struct Shape {
@@ -45,6 +45,7 @@ struct Ws {
   int32_t* grp_expert;  // [max_groups] expert of scheduling group g
   int32_t* grp_mtile0;  // [max_groups] first m-tile (within the expert) of group g
   int32_t* grp_mpre;    // [max_groups+1] prefix count of m-tiles over groups
+  int32_t* grp_ppre;    // [max_groups+1] prefix count of m-tile pairs (ceil(m-tiles / 2)) over groups
   int32_t* perm_src;    // [N]
   int32_t* perm_slot;   // [N]
   float* gate_perm;     // [N]
@@ -58,7 +59,7 @@ struct Ws {
 // Fixed layout of one workspace: byte offsets of each region.
 struct WsLayout {
   size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
-      grp_expert, grp_mtile0, grp_mpre, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
+      grp_expert, grp_mtile0, grp_mpre, grp_ppre, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
       yslot, total;
 };
 

@@ -48,15 +48,21 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(Shape s, Ws ws) {
   const int off = block_exclusive_scan(cnt, buf, &n_routed);
   const int mt = (cnt + kTileM - 1) / kTileM;
   const int ng = (mt + kGroupM - 1) / kGroupM;
-  int n_mtiles, n_groups;
+  // m-tile pairs (for CTA pairs that share a weight tile): ceil(gm / 2) per group; every
+  // group but an expert's last holds kGroupM (even) m-tiles
+  const int last_gm = mt - (ng - 1) * kGroupM;
+  const int np = ng > 0 ? (ng - 1) * (kGroupM / 2) + (last_gm + 1) / 2 : 0;
+  int n_mtiles, n_groups, n_pairs;
   const int mstart = block_exclusive_scan(mt, buf, &n_mtiles);
   const int gstart = block_exclusive_scan(ng, buf, &n_groups);
+  const int pstart = block_exclusive_scan(np, buf, &n_pairs);
 
   if (n_routed != s.N || n_groups > s.max_groups) {
     if (e == 0) record_error(ws, MOE_ERR_INTERNAL, 0x200u);
     if (e == 0) {
       ws.hdr[kHdrNumGroups] = 0;
       ws.hdr[kHdrNumMTiles] = 0;
+      ws.hdr[kHdrNumPairs] = 0;
     }
     return;
   }
@@ -72,13 +78,16 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(Shape s, Ws ws) {
       ws.grp_expert[gstart + g] = e;
       ws.grp_mtile0[gstart + g] = g * kGroupM;
       ws.grp_mpre[gstart + g] = mstart + g * kGroupM;
+      ws.grp_ppre[gstart + g] = pstart + g * (kGroupM / 2);
     }
   }
   if (e == 0) {
     ws.offsets[E] = n_routed;
     ws.grp_mpre[n_groups] = n_mtiles;
+    ws.grp_ppre[n_groups] = n_pairs;
     ws.hdr[kHdrNumGroups] = (uint32_t)n_groups;
     ws.hdr[kHdrNumMTiles] = (uint32_t)n_mtiles;
+    ws.hdr[kHdrNumPairs] = (uint32_t)n_pairs;
   }
 
   // aux = E * sum_e f_e * P_e, reduced over a fixed tree (deterministic)

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = range(6)
 MOE_F32, MOE_BF16 = 0, 1
-MOE_PATH_AUTO, MOE_PATH_SIMT = 0, 1
+MOE_PATH_AUTO, MOE_PATH_SIMT, MOE_PATH_TC_1SM = 0, 1, 2
+_PATHS = {"auto": MOE_PATH_AUTO, "simt": MOE_PATH_SIMT, "tc1": MOE_PATH_TC_1SM}
 MOE_FLAG_KEEP_LOGITS, MOE_FLAG_TEST_STALL = 1, 2
 
 if not os.path.exists(LIB_PATH):
@@ -106,7 +107,7 @@ class MoEPlan:
         out = act if out_dtype is None else (MOE_BF16 if out_dtype == "bf16" else MOE_F32)
         flags = (MOE_FLAG_KEEP_LOGITS if keep_logits else 0) | (MOE_FLAG_TEST_STALL if test_stall else 0)
         self.cfg = MoeConfig(int(T), int(d), int(E), int(k), int(F), act, out, float(tau),
-                             1 if has_bias else 0, MOE_PATH_SIMT if path == "simt" else MOE_PATH_AUTO,
+                             1 if has_bias else 0, _PATHS[path],
                              flags, int(wait_timeout_ns))
         self.T, self.d, self.E, self.k, self.F = int(T), int(d), int(E), int(k), int(F)
         self.act_dtype, self.out_dtype = _TORCH[act], _TORCH[out]

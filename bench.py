@@ -278,27 +278,45 @@ def main():
         raise RuntimeError(f"device status {st} after warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
+    # timed region 1: whole forwards (one event pair per step; the kernels of a forward are
+    # chained with programmatic dependent launch, so nothing is placed between them)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for i in range(K):
             flush.zero_()  # L2 flush between steps, outside the events
-            for s in range(len(STAGES)):
-                ev[i][s].record(stream)
-                plan.forward_stage(s, *targs)
-            ev[i][len(STAGES)].record(stream)
+            ev_s[i].record(stream)
+            plan.forward(*targs)
+            ev_e[i].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     st = plan.device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
-    stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(K)) / K for s in range(len(STAGES))]
-    step_ms = sum(ev[i][0].elapsed_time(ev[i][len(STAGES)]) for i in range(K)) / K
+    step_ms = sum(ev_s[i].elapsed_time(ev_e[i]) for i in range(K)) / K
     max_ms = reduce_max(step_ms * K, "cuda")
     value = throughput(shape.T, K, world, max_ms)
+
+    # timed region 2: the same steps with an event between every two kernels, for the
+    # per-kernel durations (and the roofline of the dominant kernel)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        for s_ in range(len(STAGES)):
+            ev[i][s_].record(stream)
+            plan.forward_stage(s_, *targs)
+        ev[i][len(STAGES)].record(stream)
+    torch.cuda.synchronize()
+    st = plan.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the per-stage timing")
+    stage_ms = [sum(ev[i][s_].elapsed_time(ev[i][s_ + 1]) for i in range(K)) / K for s_ in range(len(STAGES))]
+    staged_step_ms = sum(ev[i][0].elapsed_time(ev[i][len(STAGES)]) for i in range(K)) / K
 
     # end to end through the host-buffer entry point: pinned x in, pinned y out, every step
     e2e = None
@@ -341,7 +359,7 @@ def main():
             "config": workload_config(shape, world),
             "grouped_gemm_tflops": gemm_tflops,
             "grouped_gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16"],
-            "stage_ms": dict(zip(STAGES, stage_ms)),
+            "stage_ms": dict(zip(STAGES, stage_ms)),  # from timed region 2
             "mover_gbs": {"permute": perm_bytes / (stage_ms[2] / 1e3) / 1e9,
                           "combine": comb_bytes / (stage_ms[5] / 1e3) / 1e9},
             "roofline": {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": g1_tflops, "peak": pk["bf16"],
@@ -350,6 +368,7 @@ def main():
                          "algorithmic": f"4*N*d*F = {g1_flops} FLOP per launch (N = T*k = {shape.N} rows)"},
             "e2e": e2e,
             "gpu_launches": len(STAGES) * K,
+            "ms_per_step_with_stage_events": staged_step_ms,
             "clocks": clk.summary(),
         }
         if not args.no_cpu_baseline and world == 1:

@@ -250,6 +250,8 @@ static moe_status check_forward_args(moe_plan_t plan, const void* x, const void*
 static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& w, void* workspace, cudaStream_t st) {
   const moe::Shape& s = plan->shape;
   const moe::Ws ws = moe::ws_bind(s, workspace);
+  // every stage after the router is chained to its predecessor (programmatic dependent launch)
+  const bool pdl = stage > 0;
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0:
@@ -257,21 +259,22 @@ static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& 
       if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
       e = plan->tc ? moe::launch_route_tc(s, ws, w, plan->timeout_ns, st) : moe::launch_route_simt(s, ws, w, st);
       break;
-    case 1: e = moe::launch_scan(s, ws, st); break;
-    case 2: e = moe::launch_permute(s, ws, w, plan->num_sms, st); break;
+    case 1: e = moe::launch_scan(s, ws, pdl, st); break;
+    case 2: e = moe::launch_permute(s, ws, w, plan->num_sms, pdl, st); break;
     case 3:
     case 4: {
       const int mode = stage == 3 ? 1 : 2;
       const bool stall = mode == 1 && (plan->cfg.flags & MOE_FLAG_TEST_STALL) != 0;
       if (plan->pair)
-        e = moe::launch_gemm_tc_pair(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, st);
+        e = moe::launch_gemm_tc_pair(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, pdl, st);
       else if (plan->tc)
-        e = moe::launch_gemm_tc(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, st);
+        e = moe::launch_gemm_tc(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, pdl, st);
       else
-        e = mode == 1 ? moe::launch_gemm1_simt(s, ws, w, plan->num_sms, st) : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, st);
+        e = mode == 1 ? moe::launch_gemm1_simt(s, ws, w, plan->num_sms, pdl, st)
+                      : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, pdl, st);
       break;
     }
-    case 5: e = moe::launch_combine(s, ws, w, plan->num_sms, st); break;
+    case 5: e = moe::launch_combine(s, ws, w, plan->num_sms, pdl, st); break;
     default: return fail(MOE_ERR_INVALID_ARG, "stage %d out of range", stage);
   }
   if (e != cudaSuccess) {

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws 
   const int vec_per_row = s.d / 8;
   const int64_t total = s.T * (int64_t)vec_per_row;
   const int4* ys = reinterpret_cast<const int4*>(ws.yslot);
+  pdl_wait();  // per-slot outputs of the down-projection
+  pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * kCombThreads) {
     const int64_t t = i / vec_per_row;
@@ -55,6 +57,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
   const int vec_per_row = s.d / 4;
   const int64_t total = s.T * (int64_t)vec_per_row;
   const float4* ys = reinterpret_cast<const float4*>(ws.yslot);
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * kCombThreads) {
     const int64_t t = i / vec_per_row;
@@ -77,20 +81,18 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
   }
 }
 
-cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st) {
+cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {
   const int64_t per = s.act_bf16 ? 8 : 4;
   int64_t blocks = (s.T * (s.d / per) + kCombThreads - 1) / kCombThreads;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (s.act_bf16) {
-    if (s.out_bf16) combine_bf16_kernel<true><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
-    else combine_bf16_kernel<false><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
-  } else {
-    if (s.out_bf16) combine_f32_kernel<true><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
-    else combine_f32_kernel<false><<<(unsigned)blocks, kCombThreads, 0, st>>>(s, ws, w);
-  }
-  return cudaGetLastError();
+  const dim3 g((unsigned)blocks), b(kCombThreads);
+  if (s.act_bf16)
+    return s.out_bf16 ? launch_kernel(combine_bf16_kernel<true>, g, b, 0, st, pdl, 1, s, ws, w)
+                      : launch_kernel(combine_bf16_kernel<false>, g, b, 0, st, pdl, 1, s, ws, w);
+  return s.out_bf16 ? launch_kernel(combine_f32_kernel<true>, g, b, 0, st, pdl, 1, s, ws, w)
+                    : launch_kernel(combine_f32_kernel<false>, g, b, 0, st, pdl, 1, s, ws, w);
 }
 
 }  // namespace moe

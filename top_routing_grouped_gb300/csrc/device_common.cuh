@@ -24,6 +24,14 @@ __device__ __forceinline__ void record_error(const Ws& ws, uint32_t code, uint32
   if (atomicCAS(&ws.hdr[kHdrStatus], 0u, code) == 0u) ws.hdr[kHdrWhere] = where;
 }
 
+// Programmatic dependent launch: the kernels of one forward are chained so that a kernel's
+// launch and prologue overlap its predecessor.  pdl_wait() blocks until every grid this one
+// depends on has completed and its memory is visible (a no-op when launched without the
+// attribute); it must precede any read of a predecessor's output.  pdl_launch_dependents()
+// lets the next kernel in the stream be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

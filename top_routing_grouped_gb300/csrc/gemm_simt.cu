@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(Shape s, Ws ws,
   const Act* A = reinterpret_cast<const Act*>(kMode == 1 ? ws.xp : ws.h);
   const Act* B = reinterpret_cast<const Act*>(kMode == 1 ? w.w1 : w.w2);
   const Act* B3 = reinterpret_cast<const Act*>(w.w3);
+  pdl_wait();  // tile table, permuted rows (or H) of the previous kernels
+  pdl_launch_dependents();
   const int ngroups = (int)ws.hdr[kHdrNumGroups];
   const int total = (int)ws.hdr[kHdrNumMTiles] * n_tiles;
 
@@ -127,20 +129,17 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(Shape s, Ws ws,
 }
 
 template <int kMode>
-static cudaError_t launch_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st) {
-  const int blocks = num_sms * 4;
-  if (s.act_bf16)
-    gemm_simt_kernel<kMode, true><<<blocks, kSimtThreads, 0, st>>>(s, ws, w);
-  else
-    gemm_simt_kernel<kMode, false><<<blocks, kSimtThreads, 0, st>>>(s, ws, w);
-  return cudaGetLastError();
+static cudaError_t launch_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {
+  const dim3 g(num_sms * 4), b(kSimtThreads);
+  return s.act_bf16 ? launch_kernel(gemm_simt_kernel<kMode, true>, g, b, 0, st, pdl, 1, s, ws, w)
+                    : launch_kernel(gemm_simt_kernel<kMode, false>, g, b, 0, st, pdl, 1, s, ws, w);
 }
 
-cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st) {
-  return launch_simt<1>(s, ws, w, num_sms, st);
+cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {
+  return launch_simt<1>(s, ws, w, num_sms, pdl, st);
 }
-cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st) {
-  return launch_simt<2>(s, ws, w, num_sms, st);
+cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {
+  return launch_simt<2>(s, ws, w, num_sms, pdl, st);
 }
 
 }  // namespace moe

@@ -84,8 +84,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bn = kMode == 1 ? kMmaN / 2 : kMmaN;      // output columns per tile
   const int n_tiles = (ncols + bn - 1) / bn;
   const int kblocks = K / kBK;
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
-  const int total = (int)ws.hdr[kHdrNumMTiles] * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -114,6 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort;
+  pdl_wait();  // the tile table and the A operand come from the previous kernels
+  pdl_launch_dependents();
+  const int ngroups = (int)ws.hdr[kHdrNumGroups];
+  const int total = (int)ws.hdr[kHdrNumMTiles] * n_tiles;
 
   // fills issued by the producer whose landing nobody may have waited for (abort path)
   uint32_t issued = 0, issued_phase = 0;
@@ -342,7 +344,7 @@ cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint
 }
 
 cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
-                           int64_t timeout_ns, bool test_stall, cudaStream_t st) {
+                           int64_t timeout_ns, bool test_stall, bool pdl, cudaStream_t st) {
   CUtensorMap mA, mB, mB3;
   cudaError_t e;
   if (mode == 1) {
@@ -352,16 +354,17 @@ cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights
     if ((e = cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
         cudaSuccess)
       return e;
-    gemm_tc_kernel<1><<<num_sms, kThreads, kSmemBytes, st>>>(mA, mB, mB3, s, ws, timeout_ns, test_stall ? 1 : 0);
+    return launch_kernel(gemm_tc_kernel<1>, dim3(num_sms), dim3(kThreads), kSmemBytes, st, pdl, 1, mA, mB, mB3, s, ws,
+                         timeout_ns, test_stall ? 1 : 0);
   } else {
     if ((e = make_tmap_bf16(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kMmaM)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(gemm_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
         cudaSuccess)
       return e;
-    gemm_tc_kernel<2><<<num_sms, kThreads, kSmemBytes, st>>>(mA, mB, mB, s, ws, timeout_ns, test_stall ? 1 : 0);
+    return launch_kernel(gemm_tc_kernel<2>, dim3(num_sms), dim3(kThreads), kSmemBytes, st, pdl, 1, mA, mB, mB, s, ws,
+                         timeout_ns, test_stall ? 1 : 0);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe

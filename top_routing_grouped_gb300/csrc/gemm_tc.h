@@ -16,11 +16,11 @@ cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint
 // 2-SM version (CTA pairs, tcgen05.mma.cta_group::2): same arguments and results.
 constexpr int kPairAccBufs = 2;  // TMEM accumulators per pair CTA (x 256 columns): double-buffered
 cudaError_t launch_gemm_tc_pair(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
-                                int64_t timeout_ns, bool test_stall, cudaStream_t st);
+                                int64_t timeout_ns, bool test_stall, bool pdl, cudaStream_t st);
 
 cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int64_t timeout_ns, cudaStream_t st);
 // mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yslot[slot] = gate * (H W2^T)
 cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
-                           int64_t timeout_ns, bool test_stall, cudaStream_t st);
+                           int64_t timeout_ns, bool test_stall, bool pdl, cudaStream_t st);
 
 }  // namespace moe

@@ -83,8 +83,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bn = kMode == 1 ? kMmaN / 2 : kMmaN;  // output columns per tile
   const int n_tiles = (ncols + bn - 1) / bn;
   const int kblocks = K / kBK;
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
-  int total = (int)ws.hdr[kHdrNumPairs] * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -116,6 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   if (threadIdx.x == 0) ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&ctl->peer_tmem_base), rank ^ 1u), tmem);
   ptx::cluster_sync();
+  pdl_wait();  // the tile table and the A operand come from the previous kernels
+  pdl_launch_dependents();
+  const int ngroups = (int)ws.hdr[kHdrNumGroups];
+  int total = (int)ws.hdr[kHdrNumPairs] * n_tiles;
   if (ctl->peer_tmem_base != tmem) {  // a pair's accumulators must sit at the same TMEM address
     if (threadIdx.x == 0) record_error(ws, MOE_ERR_INTERNAL, 0x700u + kMode);
     total = 0;
@@ -318,45 +320,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int kMode, int kAccBufs>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const Shape& s, const Ws& ws,
-                        int num_sms, int64_t timeout_ns, bool stall, cudaStream_t st) {
+                        int num_sms, int64_t timeout_ns, bool stall, bool pdl, cudaStream_t st) {
   auto kern = gemm_tc2_kernel<kMode, kAccBufs>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   // as many pairs as can be resident at once (persistent loop over pair tiles)
-  cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0 &&
-      2 * clusters < (int)cfg.gridDim.x)
-    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, a, b, b3, s, ws, timeout_ns, stall ? 1 : 0);
+  int grid = num_sms & ~1;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0 && 2 * clusters < grid)
+      grid = 2 * clusters;
+  }
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, pdl, 2, a, b, b3, s, ws, timeout_ns,
+                       stall ? 1 : 0);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc_pair(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
-                                int64_t timeout_ns, bool test_stall, cudaStream_t st) {
+                                int64_t timeout_ns, bool test_stall, bool pdl, cudaStream_t st) {
   CUtensorMap mA, mB, mB3;
   cudaError_t e;
   if (mode == 1) {
     if ((e = make_tmap_bf16(&mA, ws.xp, (uint64_t)s.N, (uint64_t)s.d, kRowsPerCta)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB, w.w1, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB3, w.w3, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
-    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, s, ws, num_sms, timeout_ns, test_stall, st);
+    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, s, ws, num_sms, timeout_ns, test_stall, pdl, st);
   }
   if ((e = make_tmap_bf16(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kRowsPerCta)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN / 2)) != cudaSuccess) return e;
-  return launch_pair<2, kPairAccBufs>(mA, mB, mB, s, ws, num_sms, timeout_ns, false, st);
+  return launch_pair<2, kPairAccBufs>(mA, mB, mB, s, ws, num_sms, timeout_ns, false, pdl, st);
 }
 
 }  // namespace moe

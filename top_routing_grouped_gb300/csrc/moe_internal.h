@@ -76,13 +76,43 @@ struct Weights {
   void* y;
 };
 
-// Kernel launchers (each returns the launch's cudaError_t).
+// Launch `kernel` on `st`; `pdl` chains it to the previous kernel of the stream with
+// programmatic dependent launch (the kernel calls pdl_wait() before reading that kernel's
+// output); `cluster_x` > 1 launches clusters of that many CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Kernel launchers (each returns the launch's cudaError_t).  `pdl`: see launch_kernel.
 cudaError_t launch_route_simt(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st);
-cudaError_t launch_scan(const Shape& s, const Ws& ws, cudaStream_t st);
-cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
-cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
-cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
-cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st);
+cudaError_t launch_scan(const Shape& s, const Ws& ws, bool pdl, cudaStream_t st);
+cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
+cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
+cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
+cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
 
 // Plan internals for entry points defined outside api.cu.
 const Shape* plan_shape(moe_plan_t plan);

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(Shape s, Ws ws
   const int esz = s.act_bf16 ? 2 : 4;
   const int vecs = s.d * esz / 16;  // 16-byte vectors per row (d * esz is a multiple of 16)
   const int k = s.k;
+  pdl_wait();  // bases of the scan, ranks and choices of the router
+  pdl_launch_dependents();
 
   for (int64_t t = warp; t < s.T; t += nwarps) {
     int64_t my_p = -1;
@@ -67,12 +69,11 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(Shape s, Ws ws
   }
 }
 
-cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int num_sms, cudaStream_t st) {
+cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {
   int64_t blocks = (s.T + kPermWarps - 1) / kPermWarps;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
-  permute_kernel<<<(unsigned)blocks, kPermWarps * 32, 0, st>>>(s, ws, w);
-  return cudaGetLastError();
+  return launch_kernel(permute_kernel, dim3((unsigned)blocks), dim3(kPermWarps * 32), 0, st, pdl, 1, s, ws, w);
 }
 
 }  // namespace moe

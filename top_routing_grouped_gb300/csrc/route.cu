@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kRouteBlock) route_simt_kernel(Shape s, Ws ws,
 
   const int r = threadIdx.x;
   const int blk = blockIdx.x;
+  pdl_launch_dependents();
   const int64_t t0 = (int64_t)blk * kRouteBlock;
   for (int e = 0; e < s.E; ++e) z_s[r * ldz + e] = 0.f;
 

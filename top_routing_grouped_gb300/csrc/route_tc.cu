@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
   const int lane = threadIdx.x & 31;
   const int blk = blockIdx.x;
   const int kblocks = s.d / kBK;
+  pdl_launch_dependents();  // the scan may be scheduled; it waits for this grid to finish
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < g.stages; ++i) {

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(Shape s, Ws ws) {
   const int e = threadIdx.x;
   const int E = s.E;
   const bool on = e < E;
+  pdl_wait();  // per-block counts and sums of the router
+  pdl_launch_dependents();
 
   int cnt = 0;
   float psum = 0.f;
@@ -102,9 +104,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(Shape s, Ws ws) {
   if (e == 0) *ws.aux = (float)E * red[0];
 }
 
-cudaError_t launch_scan(const Shape& s, const Ws& ws, cudaStream_t st) {
-  scan_kernel<<<1, kScanThreads, 0, st>>>(s, ws);
-  return cudaGetLastError();
+cudaError_t launch_scan(const Shape& s, const Ws& ws, bool pdl, cudaStream_t st) {
+  return launch_kernel(scan_kernel, dim3(1), dim3(kScanThreads), 0, st, pdl, 1, s, ws);
 }
 
 }  // namespace moe

@@ -43,6 +43,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", choices=["granularity"], default=None,
+                    help="granularity sweep at equal active FLOPs (one JSON line with every G)")
+    ap.add_argument("--perf-model", action="store_true",
+                    help="fit the operator-level model on the listed workloads, predict the sweep")
     return ap.parse_args()
 
 
@@ -200,6 +204,90 @@ def cpu_baseline(shape, inputs, target_s):
                       f"OpenMP over tokens), {t:.1f} s wall"}
 
 
+def measure_shape(shape, steps, warmup):
+    """Per-stage CUDA-event times (staged pass) and whole-forward time of one layer shape."""
+    import torch
+    from top_routing_grouped_gb300 import moe
+    from top_routing_grouped_gb300.workloads import make_inputs
+    dev = make_inputs(shape, seed=0).to("cuda")
+    plan = moe.MoEPlan.for_shape(shape)
+    ws = plan.new_workspace()
+    y = torch.empty(shape.T, shape.d, dtype=plan.out_dtype, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    a = (dev.x, dev.w_router, dev.bias, dev.w1, dev.w3, dev.w2, y, ws)
+    for _ in range(warmup):
+        plan.forward(*a)
+    whole, staged = [], [[0.0] * len(STAGES)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record()
+        plan.forward(*a)
+        evs[i][1].record()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        for s_ in range(len(STAGES)):
+            ev[i][s_].record()
+            plan.forward_stage(s_, *a)
+        ev[i][len(STAGES)].record()
+    torch.cuda.synchronize()
+    if plan.device_status(ws) != 0:
+        raise RuntimeError(f"device status error on {shape.name}")
+    step_ms = sum(b.elapsed_time(e) for b, e in evs) / steps
+    stage_ms = {st: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
+                for j, st in enumerate(STAGES)}
+    counts = plan.views(ws)["expert_counts"].cpu().tolist()
+    g_ms = stage_ms["gemm1_swiglu"] + stage_ms["gemm2_gate"]
+    out = {"workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k, "d_expert": shape.F,
+           "G": None, "tokens_per_s": shape.T / (step_ms / 1e3), "ms_per_step": step_ms,
+           "grouped_gemm_tflops": shape.expert_flops / (g_ms / 1e3) / 1e12, "stage_ms": stage_ms, "counts": counts}
+    del dev, plan, ws, y, flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_sweep(args):
+    from top_routing_grouped_gb300.workloads import granularity_sweep
+    pk = peaks()
+    rows = []
+    for sh in granularity_sweep():
+        r = measure_shape(sh, max(10, args.steps // 5), args.warmup)
+        r["G"] = 8192 // sh.F
+        r["grouped_gemm_frac_of_bf16_peak"] = r["grouped_gemm_tflops"] / pk["bf16"]
+        r.pop("counts")
+        rows.append(r)
+    print(json.dumps({"metric": METRIC, "sweep": "granularity G = d_ff/d_expert at equal active FLOPs "
+                      "(T=8192, d=2048, d_ff=8192, E=8G, k=2G)", "unit": "tokens/s", "rows": rows}), flush=True)
+
+
+def run_perf_model(args):
+    from top_routing_grouped_gb300 import perf_model as pm
+    from top_routing_grouped_gb300.workloads import SHAPES, granularity_sweep
+    steps = max(10, args.steps // 5)
+    train = [SHAPES[n] for n in ("coarse_e8", "fine_e32", "skewed_e128", "large_e64")]
+    test = granularity_sweep()
+    meas = {sh.name: measure_shape(sh, steps, args.warmup) for sh in train + test}
+    samples = [(pm.features(sh, meas[sh.name]["counts"]), meas[sh.name]["stage_ms"]) for sh in train]
+    params = pm.fit(samples)
+    report = []
+    for sh in train + test:
+        m = dict(meas[sh.name]["stage_ms"])
+        m["total"] = sum(m[st] for st in pm.STAGES)
+        pred = pm.predict(params, pm.features(sh, meas[sh.name]["counts"]))
+        err = pm.mape(pred, m)
+        report.append({"workload": sh.name, "role": "fit" if sh in train else "held out",
+                       "measured_ms": {k: round(v, 4) for k, v in m.items()},
+                       "predicted_ms": {k: round(v, 4) for k, v in pred.items()},
+                       "abs_pct_err": {k: round(100 * v, 2) for k, v in err.items()}})
+    held = [r for r in report if r["role"] == "held out"]
+    print(json.dumps({"perf_model": "t = L + work / rate per kernel, fitted on the four listed bf16 workloads",
+                      "params": {st: {"L_ms": round(L, 5), "per_unit_ms": slope} for st, (L, slope) in params.items()},
+                      "fitted_rates": pm.rates(params),
+                      "held_out_total_mape_pct": round(sum(r["abs_pct_err"]["total"] for r in held) / len(held), 2),
+                      "rows": report}), flush=True)
+
+
 def run_reference(args):
     """--impl reference: the oracle on the host cores, rank 0 only."""
     rank = int(os.environ.get("RANK", "0"))
@@ -244,6 +332,10 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    if args.perf_model:
+        return run_perf_model(args)
 
     import torch
     import torch.distributed as dist

@@ -8,7 +8,7 @@
  *   z[t,e]    = (x[t] . W_r[e] + b_e) / tau                 router linear      (§3 Structure)
  *   p[t,:]    = softmax(z[t,:])                              router softmax     (§3 Structure)
  *   idx[t,:]  = the k largest z[t,e], descending, ties to the lower e           (§3 TopK)
- *   gate[t,j] = p[t, idx[t,j]]   (not renormalised)                              (§3 G(x)_i)
+ *   gate[t,j] = p[t, idx[t,j]]   (not renormalised; MOE_FLAG_RENORM_GATES: / sum_j) (§3 G(x)_i)
  *   dispatch  = rows (t,j) in expert-contiguous order, stable in token order     (§4 Dispatch)
  *   E_e(v)    = W2_e (SiLU(W1_e v) * (W3_e v))             SwiGLU expert FFN  (§3 "FFN")
  *   y[t]      = sum_j gate[t,j] * E_{idx[t,j]}(x[t])         combine            (§3 output, §4 Combine)
@@ -66,12 +66,14 @@ typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_SIMT = 1, MOE_PATH_TC_1SM = 2 } moe_p
 #define MOE_FLAG_KEEP_LOGITS 1u /* the router also stores its fp32 logits z [T,E] in the workspace */
 #define MOE_FLAG_TEST_STALL 2u  /* test hook: the expert-GEMM producer withholds its first stage,
                                    so its consumers' bounded waits run out (MOE_ERR_TIMEOUT) */
+#define MOE_FLAG_RENORM_GATES 4u /* variant: gates renormalised over the k chosen experts
+                                    (gate[t,j] = p[t,idx[t,j]] / sum_j' p[t,idx[t,j']]) */
 
 typedef struct {
   int64_t T;                /* tokens, >= 1 */
   int32_t d_model;          /* d, >= 1 */
   int32_t n_experts;        /* E, 1..256 */
-  int32_t top_k;            /* k, 1..min(E, 8) */
+  int32_t top_k;            /* k, 1..min(E, 16) */
   int32_t d_expert;         /* F, >= 1 */
   int32_t act_dtype;        /* moe_dtype of x, W_r, W1, W3, W2 */
   int32_t out_dtype;        /* moe_dtype of y */

@@ -21,7 +21,7 @@ _lib = None
 class OracleCfg(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("tau", ctypes.c_double)]
+                ("tau", ctypes.c_double), ("renorm", ctypes.c_int32)]
 
 
 def load(path=None):
@@ -56,16 +56,17 @@ class Oracle:
 
     ``T, d, E, k, F`` as in the page's notation (tokens, model width, experts, top-k,
     expert hidden width); ``tau`` the router temperature; ``dtype`` "f32" or "bf16" for
-    how x and the weights are stored.
+    how x and the weights are stored; ``renorm`` renormalises the gates over the k chosen.
     """
 
-    def __init__(self, T, d, E, k, F, tau=1.0, dtype="f32", lib=None):
+    def __init__(self, T, d, E, k, F, tau=1.0, dtype="f32", lib=None, renorm=False):
         self.T, self.d, self.E, self.k, self.F = int(T), int(d), int(E), int(k), int(F)
         self.tau = float(tau)
         self.dtype = dtype
         self.lib = lib if lib is not None else load()
+        self.renorm = bool(renorm)
         self.cfg = OracleCfg(self.T, self.d, self.E, self.k, self.F,
-                             1 if dtype == "bf16" else 0, self.tau)
+                             1 if dtype == "bf16" else 0, self.tau, 1 if renorm else 0)
 
     # -- helpers -----------------------------------------------------------------
     def _in(self, a):

@@ -44,6 +44,7 @@ typedef struct {
   int32_t F;     /* d_expert: hidden width of one expert */
   int32_t dtype; /* storage of x and weights: 0 = fp32, 1 = bf16 bit patterns */
   double tau;    /* router temperature, > 0 */
+  int32_t renorm; /* 0: gates are the chosen softmax entries; 1: renormalised over the k chosen */
 } orc_cfg;
 
 /* Element i of a fp32 or bf16 array, widened exactly to double. */
@@ -59,7 +60,7 @@ static double orc_load(const void* base, int32_t dtype, int64_t i) {
 
 static int orc_check(const orc_cfg* c) {
   if (!c || c->T < 0 || c->d <= 0 || c->E <= 0 || c->k <= 0 || c->k > c->E || c->F <= 0 ||
-      !(c->tau > 0.0) || (c->dtype != 0 && c->dtype != 1))
+      !(c->tau > 0.0) || (c->dtype != 0 && c->dtype != 1) || (c->renorm != 0 && c->renorm != 1))
     return ORC_BAD_ARG;
   return ORC_OK;
 }
@@ -72,6 +73,8 @@ static int orc_check(const orc_cfg* c) {
  *   idx[t,:] = the k experts with the largest fp32-rounded z, descending, ties to the
  *              lower index
  *   gate[t,j]= p[t, idx[t,j]]
+ * or, with renorm (a variant the page's TopK leaves open), the same entries divided by
+ * their sum over the k chosen (summed in j order), i.e. a softmax over the chosen logits.
  * bias may be NULL (no bias).  Any of z, p may be NULL when not wanted.
  */
 int orc_router(const orc_cfg* c, const void* x, const void* wr, const float* bias, double* z,
@@ -124,6 +127,11 @@ int orc_router(const orc_cfg* c, const void* x, const void* wr, const float* bia
           taken[best] = 1;
           idx[t * k + j] = best;
           gate[t * k + j] = pt[best];
+        }
+        if (c->renorm) {
+          double chosen = 0.0;
+          for (int32_t j = 0; j < k; ++j) chosen += gate[t * k + j];
+          for (int32_t j = 0; j < k; ++j) gate[t * k + j] /= chosen;
         }
         if (z)
           for (int32_t e = 0; e < E; ++e) z[t * E + e] = zt[e];

@@ -94,8 +94,10 @@ def check_routing(orc, host, bias, got, rep):
     gz = np.take_along_axis(zs32, gidx, axis=1).astype(np.float64)
     assert np.all(gz[:, :-1] - gz[:, 1:] >= -MARGIN), "chosen experts not in descending logit order"
     rep.add("slots in oracle order", f"{int(np.all(gidx == oidx, axis=1).sum())}/{T}")
-    # gates: the oracle's softmax at the GPU's indices
+    # gates: the oracle's softmax at the GPU's indices (renormalised over them in that variant)
     gref = np.take_along_axis(p, gidx, axis=1)
+    if getattr(orc, "renorm", False):
+        gref = gref / gref.sum(axis=1, keepdims=True)
     gerr = np.abs(ggate - gref) / (gref + GATE_FLOOR)
     rep.add("gate max rel err", float(gerr.max()))
     assert gerr.max() <= GATE_RTOL, f"gates off by {gerr.max()}"
@@ -157,7 +159,8 @@ def full_check(shape, inputs, plan, y_tokens=None, h_rows=None, seed=0):
     host = inputs.numpy_for_oracle()
     dev = inputs.to("cuda")
     got = run_gpu(plan, dev)
-    orc = oracle.Oracle(shape.T, shape.d, shape.E, shape.k, shape.F, tau=shape.tau, dtype=shape.dtype)
+    orc = oracle.Oracle(shape.T, shape.d, shape.E, shape.k, shape.F, tau=shape.tau, dtype=shape.dtype,
+                        renorm=getattr(plan, "renorm_gates", False))
     bias = host["bias"]
     z, p, gidx, gref, perm_src, perm_slot, counts, offsets = check_routing(orc, host, bias, got, rep)
     check_xp(dev.x, got, perm_src)

@@ -60,7 +60,7 @@ def test_plan_workspace_and_stages(moe):
     (dict(T=0), "MOE_ERR_INVALID_ARG"),
     (dict(E=0), "MOE_ERR_INVALID_ARG"),
     (dict(E=300), "MOE_ERR_INVALID_ARG"),
-    (dict(k=9, E=16), "MOE_ERR_INVALID_ARG"),
+    (dict(k=17, E=32), "MOE_ERR_INVALID_ARG"),
     (dict(k=5, E=4), "MOE_ERR_INVALID_ARG"),
     (dict(tau=0.0), "MOE_ERR_INVALID_ARG"),
     (dict(tau=float("inf")), "MOE_ERR_INVALID_ARG"),

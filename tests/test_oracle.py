@@ -184,8 +184,25 @@ def pin_expert_rows(lib):
             np.testing.assert_allclose(out, w2[e] @ href, rtol=1e-11, atol=1e-13)
 
 
+def pin_renormalised_gates(lib):
+    """Variant: gates renormalised over the k chosen = a softmax over the chosen logits."""
+    s = shape(T=60, d=16, E=8, k=3, F=8, tau=0.8)
+    inp = make_inputs(s, seed=12).numpy_for_oracle()
+    o = oracle.Oracle(s.T, s.d, s.E, s.k, s.F, tau=s.tau, lib=lib, renorm=True)
+    z, p, idx, gate = o.router(inp["x"], inp["wr"])
+    zc = np.take_along_axis(z, idx, axis=1)
+    np.testing.assert_allclose(gate, scipy.special.softmax(zc, axis=1), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(gate.sum(axis=1), 1.0, atol=1e-14)
+    # k = 1: the single gate is exactly 1; k = E: the renormalised gates are the softmax itself
+    o1 = oracle.Oracle(s.T, s.d, s.E, 1, s.F, tau=s.tau, lib=lib, renorm=True)
+    assert np.all(o1.router(inp["x"], inp["wr"])[3] == 1.0)
+    oE = oracle.Oracle(s.T, s.d, s.E, s.E, s.F, tau=s.tau, lib=lib, renorm=True)
+    _, pE, idxE, gE = oE.router(inp["x"], inp["wr"])
+    np.testing.assert_allclose(gE, np.take_along_axis(pE, idxE, axis=1), rtol=1e-12)
+
+
 PINS = [pin_dense_reduction, pin_router_library, pin_bruteforce, pin_invariants, pin_golden,
-        pin_aux, pin_expert_rows]
+        pin_aux, pin_expert_rows, pin_renormalised_gates]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -249,6 +266,9 @@ MUTANTS = {
     "aux_without_k": ("double f = (double)counts[i] / ((double)T * (double)c->k);",
                       "double f = (double)counts[i] / (double)T;"),
     "softmax_unnormalised": ("for (int32_t e = 0; e < E; ++e) pt[e] /= s;", ""),
+    "renorm_ignored": ("if (c->renorm) {", "if (0) {"),
+    "renorm_over_all": ("for (int32_t j = 0; j < k; ++j) chosen += gate[t * k + j];",
+                        "for (int32_t e = 0; e < E; ++e) chosen += pt[e];"),
 }
 
 

@@ -30,7 +30,7 @@ def check(moe, shape, inputs, path="auto", y_tokens=None, h_rows=None, has_bias=
     import parity
     plan = moe.MoEPlan(shape.T, shape.d, shape.E, shape.k, shape.F, dtype=shape.dtype, tau=shape.tau,
                        has_bias=(inputs.bias is not None) if has_bias is None else has_bias,
-                       path=path, keep_logits=True)
+                       path=path, keep_logits=True, renorm_gates=shape.renorm)
     rep, got = parity.full_check(shape, inputs, plan, y_tokens=y_tokens, h_rows=h_rows)
     print(f"\n[{shape.name} path={path}]\n{rep}")
     return rep, got
@@ -113,6 +113,23 @@ def test_deterministic(moe, path):
     b = parity.run_gpu(plan, dev)
     assert torch.equal(a["y"], b["y"])
     assert a["aux"] == b["aux"]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dims", [
+    (300, 256, 8, 1, 128),     # k = 1 (Switch-style routing)
+    (256, 128, 32, 16, 64),    # k = 16, the largest top-k
+    (200, 128, 8, 4, 128),
+], ids=lambda d: "x".join(map(str, d)))
+@pytest.mark.parametrize("renorm", [False, True], ids=["softmax_gates", "renorm_gates"])
+def test_variants(moe, path, dims, renorm):
+    """Variants the page leaves open: k = 1, large k, gates renormalised over the chosen."""
+    T, d, E, k, F = dims
+    s = small("variant", T, d, E, k, F).with_(renorm=renorm)
+    rep, got = check(moe, s, make_inputs(s, seed=7), path=path)
+    if renorm:
+        g = got["views"]["topk_gate"].cpu().double()
+        assert torch.allclose(g.sum(dim=1), torch.ones(T, dtype=torch.float64), atol=1e-6)
 
 
 def smallest_expert_tokens(got, cap=48):

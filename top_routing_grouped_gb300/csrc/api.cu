@@ -177,7 +177,8 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
   if (c.has_router_bias != 0 && c.has_router_bias != 1) return fail(MOE_ERR_INVALID_ARG, "has_router_bias must be 0 or 1");
   if (c.path != MOE_PATH_AUTO && c.path != MOE_PATH_SIMT && c.path != MOE_PATH_TC_1SM)
     return fail(MOE_ERR_INVALID_ARG, "bad path");
-  if (c.flags & ~(MOE_FLAG_KEEP_LOGITS | MOE_FLAG_TEST_STALL)) return fail(MOE_ERR_INVALID_ARG, "unknown flags");
+  if (c.flags & ~(MOE_FLAG_KEEP_LOGITS | MOE_FLAG_TEST_STALL | MOE_FLAG_RENORM_GATES))
+    return fail(MOE_ERR_INVALID_ARG, "unknown flags");
   const int64_t N = c.T * (int64_t)c.top_k;
   if (N > (int64_t)INT32_MAX / 2 || N * (int64_t)(c.d_model > c.d_expert ? c.d_model : c.d_expert) > ((int64_t)1 << 40))
     return fail(MOE_ERR_UNSUPPORTED, "T * top_k (or the routed activations) too large");
@@ -205,6 +206,7 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
   s.tau = c.router_temperature;
   s.has_bias = c.has_router_bias;
   s.keep_logits = (c.flags & MOE_FLAG_KEEP_LOGITS) ? 1 : 0;
+  s.renorm = (c.flags & MOE_FLAG_RENORM_GATES) ? 1 : 0;
   s.act_bf16 = bf16 ? 1 : 0;
   s.out_bf16 = c.out_dtype == MOE_BF16 ? 1 : 0;
   // groups of up to kGroupM m-tiles per expert: sum_e ceil(mt_e / G) <= MT / G + E and

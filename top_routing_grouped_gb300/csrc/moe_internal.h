@@ -10,7 +10,7 @@ namespace moe {
 constexpr int kRouteBlock = 128;   // tokens per router CTA (= rows of one router MMA tile)
 constexpr int kTileM = 128;        // rows per expert-GEMM m-tile
 constexpr int kGroupM = 8;         // m-tiles per scheduling group (weight-tile reuse in L2)
-constexpr int kMaxTopK = 8;
+constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 256;
 
 // Status word slots in the workspace header.
@@ -25,6 +25,7 @@ struct Shape {
   float tau;
   int has_bias;
   int keep_logits;
+  int renorm;     // gates renormalised over the k chosen
   int act_bf16;   // x and weights are bf16 (else fp32)
   int out_bf16;   // y is bf16 (else fp32)
   int max_groups; // capacity of the group table

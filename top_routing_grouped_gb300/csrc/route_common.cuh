@@ -15,7 +15,8 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 // z_s[r * ldz + e] holds the finished logit z = (x.W_r[e] + b_e)/tau of token blk*128 + r.
 //   1. per token: p = softmax(z) (fp32, expf), top-k by descending z with ties to the
 //      lower expert (a fixed insertion network over kMaxTopK slots, strict '>'),
-//      gates p[idx]; writes topk_idx / topk_gate (and the logits when kept);
+//      gates p[idx] (divided by their sum over the k chosen in the renormalised variant);
+//      writes topk_idx / topk_gate (and the logits when kept);
 //   2. per block: for every expert, a bitmask of the block's tokens that chose it; the
 //      slot's rank among the block's slots of the same expert is the popcount of the
 //      tokens before it (stable in token order, deterministic);
@@ -84,12 +85,19 @@ __device__ __forceinline__ void route_finish(const Shape& s, const Ws& ws, int b
       sum += q;
     }
     for (int e = 0; e < E; ++e) zr[e] = zr[e] / sum;
+    float chosen = 1.f;  // sum of the chosen entries, in slot order (renormalised variant)
+    if (s.renorm) {
+      chosen = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j < k) chosen += zr[bi[j]];
+    }
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j < k) {
         const int e = bi[j];
         ws.topk_idx[t * k + j] = e;
-        ws.topk_gate[t * k + j] = zr[e];
+        ws.topk_gate[t * k + j] = s.renorm ? zr[e] / chosen : zr[e];
         atomicOr(&mask_s[e * 4 + (r >> 5)], 1u << (r & 31));
       }
     }

@@ -17,7 +17,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT,
 MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_SIMT, MOE_PATH_TC_1SM = 0, 1, 2
 _PATHS = {"auto": MOE_PATH_AUTO, "simt": MOE_PATH_SIMT, "tc1": MOE_PATH_TC_1SM}
-MOE_FLAG_KEEP_LOGITS, MOE_FLAG_TEST_STALL = 1, 2
+MOE_FLAG_KEEP_LOGITS, MOE_FLAG_TEST_STALL, MOE_FLAG_RENORM_GATES = 1, 2, 4
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -102,10 +102,12 @@ class MoEPlan:
     top-k, F = d_expert, router temperature tau)."""
 
     def __init__(self, T, d, E, k, F, dtype="bf16", out_dtype=None, tau=1.0, has_bias=False,
-                 path="auto", keep_logits=False, test_stall=False, wait_timeout_ns=0):
+                 path="auto", keep_logits=False, test_stall=False, wait_timeout_ns=0, renorm_gates=False):
         act = MOE_BF16 if dtype == "bf16" else MOE_F32
         out = act if out_dtype is None else (MOE_BF16 if out_dtype == "bf16" else MOE_F32)
-        flags = (MOE_FLAG_KEEP_LOGITS if keep_logits else 0) | (MOE_FLAG_TEST_STALL if test_stall else 0)
+        flags = ((MOE_FLAG_KEEP_LOGITS if keep_logits else 0) | (MOE_FLAG_TEST_STALL if test_stall else 0)
+                 | (MOE_FLAG_RENORM_GATES if renorm_gates else 0))
+        self.renorm_gates = bool(renorm_gates)
         self.cfg = MoeConfig(int(T), int(d), int(E), int(k), int(F), act, out, float(tau),
                              1 if has_bias else 0, _PATHS[path],
                              flags, int(wait_timeout_ns))
@@ -118,6 +120,7 @@ class MoEPlan:
 
     @classmethod
     def for_shape(cls, shape, **kw):
+        kw.setdefault("renorm_gates", shape.renorm)
         return cls(shape.T, shape.d, shape.E, shape.k, shape.F, dtype=shape.dtype, tau=shape.tau,
                    has_bias=shape.zipf_bias, **kw)
 

@@ -32,6 +32,7 @@ class MoEShape:
     dtype: str      # "f32" or "bf16": storage and input type of x and the weights
     tau: float = 1.0
     zipf_bias: bool = False
+    renorm: bool = False   # variant: gates renormalised over the k chosen
     note: str = ""
 
     @property
@@ -64,6 +65,14 @@ SHAPES = {
 
 # The order the workloads are listed in: tiny fp32, coarse, fine, skewed, large.
 ORDER = ["tiny_f32", "coarse_e8", "fine_e32", "skewed_e128", "large_e64"]
+
+
+def granularity_sweep(T=8192, d=2048, d_ff=8192, base_experts=8, base_k=2, Gs=(1, 2, 4, 8)):
+    """Layers of equal active FLOPs and equal total expert parameters that differ only in
+    granularity G = d_ff / d_expert ("Compute-Optimal Is Not Cluster-Optimal", the 4-D
+    scaling law's G): E = base_experts * G experts of width d_ff / G, top-(base_k * G)."""
+    return [MoEShape(f"granularity_g{G}", T=T, d=d, E=base_experts * G, k=base_k * G, F=d_ff // G,
+                     dtype="bf16", note=f"granularity G={G}") for G in Gs]
 
 
 @dataclass

@@ -42,9 +42,10 @@ def load(path=None):
     lib.orc_combine.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_int64, P]
     lib.orc_aux.argtypes = [cfgp, P, P, P]
     lib.orc_forward.argtypes = [cfgp] + [P] * 16
+    lib.orc_backward.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_double, P, P, P, P, P, P]
     lib.orc_num_threads.argtypes = []
     for f in ("orc_router", "orc_dispatch", "orc_expert", "orc_combine", "orc_aux",
-              "orc_forward", "orc_num_threads"):
+              "orc_forward", "orc_num_threads", "orc_backward"):
         getattr(lib, f).restype = ctypes.c_int
     if path is None or path == _build.LIB:
         _lib = lib
@@ -160,6 +161,21 @@ class Oracle:
                    self._p(r["perm_slot"]), self._p(r["z"]), self._p(r["p"]),
                    ctypes.byref(aux))
         r["aux"] = aux.value
+        return r
+
+
+    def backward(self, x, wr, bias, w1, w3, w2, dy, alpha=0.0):
+        """Gradients of L = sum(dy * y) + alpha * aux: dict dx [T,d], dwr [E,d], dbias [E],
+        dw1, dw3 [E,F,d], dw2 [E,d,F] (fp64)."""
+        T, E, d, F = self.T, self.E, self.d, self.F
+        r = dict(dx=np.empty((T, d)), dwr=np.empty((E, d)), dbias=np.empty(E), dw1=np.empty((E, F, d)),
+                 dw3=np.empty((E, F, d)), dw2=np.empty((E, d, F)))
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        dy = np.ascontiguousarray(dy, dtype=np.float64)
+        self._call("orc_backward", self._p(self._in(x)), self._p(self._in(wr)), self._p(b),
+                   self._p(self._in(w1)), self._p(self._in(w3)), self._p(self._in(w2)), self._p(dy),
+                   float(alpha), self._p(r["dx"]), self._p(r["dwr"]), self._p(r["dbias"]),
+                   self._p(r["dw1"]), self._p(r["dw3"]), self._p(r["dw2"]))
         return r
 
 

@@ -337,3 +337,184 @@ int orc_num_threads(void) {
   }
   return n;
 }
+
+/*
+ * Backward of the layer for the scalar  L = sum_t dy[t] . y[t] + alpha * aux
+ * (the page's training setting: the balancing loss is added to the task loss; alpha is its
+ * weight).  Routing (top-k choice, counts f_i) is piecewise constant and carries no
+ * gradient; the gradient reaches the router through the gate values and through P_i.
+ *   per slot (t, j), e = idx, g = gate:
+ *     a = W1_e x, b = W3_e x, h = silu(a) b, o = W2_e h
+ *     dg  = dy . o                      do = g dy
+ *     dW2_e += do h^T                   dh = W2_e^T do
+ *     da = dh * b * silu'(a)            db = dh * silu(a),  silu'(a) = s (1 + a (1 - s)), s = sigmoid(a)
+ *     dW1_e += da x^T,  dW3_e += db x^T,  dx += W1_e^T da + W3_e^T db
+ *   router, per token: dp_e = sum_j [idx_j = e] dg_j  (renormalised gates: dp at the chosen
+ *     = (dg_j - sum_j' g_j' dg_j') / S, S = sum of the chosen p)  + alpha E f_e / T
+ *     dz = p * (dp - sum_e p_e dp_e),  dl = dz / tau
+ *     dW_r[e] += dl_e x,  dbias_e += dl_e,  dx += sum_e dl_e W_r[e]
+ * Outputs (host, fp64): dx [T,d], dwr [E,d], dbias [E], dw1, dw3 [E,F,d], dw2 [E,d,F].
+ * Weight gradients are summed over tokens in token order (OpenMP over experts).
+ */
+int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* bias, const void* w1, const void* w3,
+                 const void* w2, const double* dy, double alpha, double* dx, double* dwr, double* dbias,
+                 double* dw1, double* dw3, double* dw2) {
+  if (orc_check(c) || !x || !wr || !w1 || !w3 || !w2 || !dy || !dx || !dwr || !dbias || !dw1 || !dw3 || !dw2)
+    return ORC_BAD_ARG;
+  const int64_t T = c->T, N = c->T * c->k;
+  const int32_t d = c->d, E = c->E, k = c->k, F = c->F;
+  double* p = (double*)malloc(sizeof(double) * (size_t)(T * E));
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  double* gate = (double*)malloc(sizeof(double) * (size_t)N);
+  int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+  int32_t* offsets = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
+  double* sa = (double*)malloc(sizeof(double) * (size_t)(N * F)); /* per slot: da */
+  double* sb = (double*)malloc(sizeof(double) * (size_t)(N * F)); /* db */
+  double* sh = (double*)malloc(sizeof(double) * (size_t)(N * F)); /* h */
+  double* dg = (double*)malloc(sizeof(double) * (size_t)N);
+  int rc = ORC_OK;
+  if (!p || !idx || !gate || !counts || !offsets || !sa || !sb || !sh || !dg) rc = ORC_NO_MEM;
+  if (!rc) rc = orc_router(c, x, wr, bias, NULL, p, idx, gate);
+  if (!rc) rc = orc_dispatch(c, idx, counts, offsets, NULL, NULL);
+  int failed = 0;
+  if (!rc) {
+#pragma omp parallel
+    {
+      double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+      double* av = (double*)malloc(sizeof(double) * (size_t)F);
+      double* bv = (double*)malloc(sizeof(double) * (size_t)F);
+      double* dh = (double*)malloc(sizeof(double) * (size_t)F);
+      double* o = (double*)malloc(sizeof(double) * (size_t)d);
+      double* dp = (double*)malloc(sizeof(double) * (size_t)E);
+      if (!xr || !av || !bv || !dh || !o || !dp) {
+#pragma omp atomic write
+        failed = 1;
+      } else {
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+          double* dxt = dx + t * d;
+          for (int32_t col = 0; col < d; ++col) {
+            xr[col] = orc_load(x, c->dtype, t * d + col);
+            dxt[col] = 0.0;
+          }
+          const double* dyt = dy + t * d;
+          for (int32_t j = 0; j < k; ++j) {
+            const int64_t slot = t * k + j;
+            const int32_t e = idx[slot];
+            const int64_t wb = (int64_t)e * F * d;
+            double* h = sh + slot * F;
+            for (int32_t f = 0; f < F; ++f) {
+              double a = 0.0, b = 0.0;
+              for (int32_t col = 0; col < d; ++col) {
+                a += orc_load(w1, c->dtype, wb + (int64_t)f * d + col) * xr[col];
+                b += orc_load(w3, c->dtype, wb + (int64_t)f * d + col) * xr[col];
+              }
+              av[f] = a;
+              bv[f] = b;
+              h[f] = a / (1.0 + exp(-a)) * b;
+            }
+            double g = gate[slot], dgs = 0.0;
+            for (int32_t r = 0; r < d; ++r) {
+              double acc = 0.0;
+              for (int32_t f = 0; f < F; ++f) acc += orc_load(w2, c->dtype, wb + (int64_t)r * F + f) * h[f];
+              o[r] = acc;
+              dgs += dyt[r] * acc;
+            }
+            dg[slot] = dgs;
+            for (int32_t f = 0; f < F; ++f) {
+              double acc = 0.0;
+              for (int32_t r = 0; r < d; ++r) acc += orc_load(w2, c->dtype, wb + (int64_t)r * F + f) * g * dyt[r];
+              dh[f] = acc;
+            }
+            double* da = sa + slot * F;
+            double* db = sb + slot * F;
+            for (int32_t f = 0; f < F; ++f) {
+              const double s = 1.0 / (1.0 + exp(-av[f]));
+              da[f] = dh[f] * bv[f] * s * (1.0 + av[f] * (1.0 - s));
+              db[f] = dh[f] * av[f] * s;
+            }
+            for (int32_t col = 0; col < d; ++col) {
+              double acc = 0.0;
+              for (int32_t f = 0; f < F; ++f)
+                acc += orc_load(w1, c->dtype, wb + (int64_t)f * d + col) * da[f] +
+                       orc_load(w3, c->dtype, wb + (int64_t)f * d + col) * db[f];
+              dxt[col] += acc;
+            }
+          }
+          /* router */
+          const double* pt = p + t * E;
+          for (int32_t e = 0; e < E; ++e) dp[e] = alpha * (double)E * (double)counts[e] / ((double)T * (double)k) / (double)T;
+          if (c->renorm) {
+            double S = 0.0, gdg = 0.0;
+            for (int32_t j = 0; j < k; ++j) S += pt[idx[t * k + j]];
+            for (int32_t j = 0; j < k; ++j) gdg += gate[t * k + j] * dg[t * k + j];
+            for (int32_t j = 0; j < k; ++j) dp[idx[t * k + j]] += (dg[t * k + j] - gdg) / S;
+          } else {
+            for (int32_t j = 0; j < k; ++j) dp[idx[t * k + j]] += dg[t * k + j];
+          }
+          double pdp = 0.0;
+          for (int32_t e = 0; e < E; ++e) pdp += pt[e] * dp[e];
+          for (int32_t e = 0; e < E; ++e) {
+            const double dl = pt[e] * (dp[e] - pdp) / c->tau;
+            dp[e] = dl; /* reuse: dlogit */
+            for (int32_t col = 0; col < d; ++col) dxt[col] += dl * orc_load(wr, c->dtype, (int64_t)e * d + col);
+          }
+          for (int32_t e = 0; e < E; ++e) p[t * E + e] = dp[e]; /* keep dlogit for the router weights */
+        }
+      }
+      free(xr);
+      free(av);
+      free(bv);
+      free(dh);
+      free(o);
+      free(dp);
+    }
+    if (failed) rc = ORC_NO_MEM;
+  }
+  if (!rc) {
+    /* weight gradients, per expert in token order (p now holds dlogit [T,E]) */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t e = 0; e < E; ++e) {
+      double* g1 = dw1 + (int64_t)e * F * d;
+      double* g3 = dw3 + (int64_t)e * F * d;
+      double* g2 = dw2 + (int64_t)e * d * F;
+      memset(g1, 0, sizeof(double) * (size_t)F * d);
+      memset(g3, 0, sizeof(double) * (size_t)F * d);
+      memset(g2, 0, sizeof(double) * (size_t)d * F);
+      double* gr = dwr + (int64_t)e * d;
+      memset(gr, 0, sizeof(double) * (size_t)d);
+      dbias[e] = 0.0;
+      for (int64_t t = 0; t < T; ++t) {
+        const double dl = p[t * E + e];
+        for (int32_t col = 0; col < d; ++col) gr[col] += dl * orc_load(x, c->dtype, t * d + col);
+        dbias[e] += dl;
+        for (int32_t j = 0; j < k; ++j) {
+          const int64_t slot = t * k + j;
+          if (idx[slot] != e) continue;
+          const double* da = sa + slot * F;
+          const double* db = sb + slot * F;
+          const double* h = sh + slot * F;
+          const double g = gate[slot];
+          for (int32_t f = 0; f < F; ++f)
+            for (int32_t col = 0; col < d; ++col) {
+              const double xv = orc_load(x, c->dtype, t * d + col);
+              g1[(int64_t)f * d + col] += da[f] * xv;
+              g3[(int64_t)f * d + col] += db[f] * xv;
+            }
+          for (int32_t r = 0; r < d; ++r)
+            for (int32_t f = 0; f < F; ++f) g2[(int64_t)r * F + f] += g * dy[t * d + r] * h[f];
+        }
+      }
+    }
+  }
+  free(p);
+  free(idx);
+  free(gate);
+  free(counts);
+  free(offsets);
+  free(sa);
+  free(sb);
+  free(sh);
+  free(dg);
+  return rc;
+}

@@ -66,6 +66,9 @@ typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_SIMT = 1, MOE_PATH_TC_1SM = 2 } moe_p
 #define MOE_FLAG_KEEP_LOGITS 1u /* the router also stores its fp32 logits z [T,E] in the workspace */
 #define MOE_FLAG_TEST_STALL 2u  /* test hook: the expert-GEMM producer withholds its first stage,
                                    so its consumers' bounded waits run out (MOE_ERR_TIMEOUT) */
+#define MOE_FLAG_TRAINING 8u     /* the forward also keeps what moe_backward needs (the two
+                                    pre-activations of every routed row and the router softmax);
+                                    bf16 tensor-core plans with bf16 output */
 #define MOE_FLAG_RENORM_GATES 4u /* variant: gates renormalised over the k chosen experts
                                     (gate[t,j] = p[t,idx[t,j]] / sum_j' p[t,idx[t,j']]) */
 
@@ -140,6 +143,22 @@ moe_status moe_forward_host(moe_plan_t plan, const void* x_host, void* x_dev, co
                             const float* router_bias, const void* w1, const void* w3, const void* w2,
                             void* y_dev, void* y_host, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/* Backward of the layer for the loss  L = sum_t dy[t] . y[t] + aux_weight * aux  (the page's
+ * training setting, §3 Load-Balancing Loss: the balancing loss is added to the training loss
+ * and reaches mainly the router).  Needs a plan made with MOE_FLAG_TRAINING and the workspace
+ * of the last moe_forward of that plan on the same x and weights.  The routing (top-k
+ * choice, counts) is piecewise constant and passes no gradient; the router receives it
+ * through the gate values and through the softmax mean P_e.
+ *   dy [T,d]: in the plan's out_dtype.
+ *   outputs (fp32, device): dx [T,d]; dw_router [E,d]; dbias [E] (only if the plan has a
+ *   bias, may be NULL otherwise); dw1, dw3 [E,F,d]; dw2 [E,d,F].  Every output is written
+ *   completely (experts with no routed rows get zero weight gradients).
+ * Asynchronous on `stream`; device-side waits are bounded as for moe_forward. */
+moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
+                        const void* w1, const void* w3, const void* w2, const void* dy, float aux_weight, float* dx,
+                        float* dw_router, float* dbias, float* dw1, float* dw3, float* dw2, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /* Copy the balancing scalar aux = E * sum_e f_e P_e of the last forward on `workspace`
  * to the device float *aux_out (stream-ordered, asynchronous).  (§3 Load-Balancing Loss) */

@@ -266,7 +266,7 @@ MUTANTS = {
     "aux_without_k": ("double f = (double)counts[i] / ((double)T * (double)c->k);",
                       "double f = (double)counts[i] / (double)T;"),
     "softmax_unnormalised": ("for (int32_t e = 0; e < E; ++e) pt[e] /= s;", ""),
-    "renorm_ignored": ("if (c->renorm) {", "if (0) {"),
+    "renorm_ignored": ("for (int32_t j = 0; j < k; ++j) gate[t * k + j] /= chosen;", ""),
     "renorm_over_all": ("for (int32_t j = 0; j < k; ++j) chosen += gate[t * k + j];",
                         "for (int32_t e = 0; e < E; ++e) chosen += pt[e];"),
 }

@@ -103,6 +103,20 @@ WsLayout ws_layout(const Shape& s) {
   L.xp = take(N * (size_t)s.d * esz);
   L.h = take(N * (size_t)s.F * esz);
   L.yslot = take(N * (size_t)s.d * esz);
+  if (s.training) {
+    const size_t nt = ((size_t)s.F + 255) / 256, chunks = ((size_t)s.T + 255) / 256;
+    L.a1 = take(N * (size_t)s.F * 2);
+    L.a3 = take(N * (size_t)s.F * 2);
+    L.probs = take((size_t)s.T * E * 4);
+    L.dyp = take(N * (size_t)s.d * 2);
+    L.dop = take(N * (size_t)s.d * 2);
+    L.dab = take(N * 2 * (size_t)s.F * 2);
+    L.dgp = take(N * nt * 4);
+    L.dxslot = take(N * (size_t)s.d * 2);
+    L.dlogit = take((size_t)s.T * E * 4);
+    L.dwr_part = take(chunks * E * (size_t)s.d * 4);
+    L.dwr_part_b = take(chunks * E * 4);
+  }
   L.total = off;
   return L;
 }
@@ -133,6 +147,19 @@ Ws ws_bind(const Shape& s, void* base) {
   w.xp = b + L.xp;
   w.h = b + L.h;
   w.yslot = b + L.yslot;
+  if (s.training) {
+    w.a1 = b + L.a1;
+    w.a3 = b + L.a3;
+    w.probs = reinterpret_cast<float*>(b + L.probs);
+    w.dyp = b + L.dyp;
+    w.dop = b + L.dop;
+    w.dab = b + L.dab;
+    w.dgp = reinterpret_cast<float*>(b + L.dgp);
+    w.dxslot = b + L.dxslot;
+    w.dlogit = reinterpret_cast<float*>(b + L.dlogit);
+    w.dwr_part = reinterpret_cast<float*>(b + L.dwr_part);
+    w.dwr_part_b = reinterpret_cast<float*>(b + L.dwr_part_b);
+  }
   return w;
 }
 
@@ -177,7 +204,7 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
   if (c.has_router_bias != 0 && c.has_router_bias != 1) return fail(MOE_ERR_INVALID_ARG, "has_router_bias must be 0 or 1");
   if (c.path != MOE_PATH_AUTO && c.path != MOE_PATH_SIMT && c.path != MOE_PATH_TC_1SM)
     return fail(MOE_ERR_INVALID_ARG, "bad path");
-  if (c.flags & ~(MOE_FLAG_KEEP_LOGITS | MOE_FLAG_TEST_STALL | MOE_FLAG_RENORM_GATES))
+  if (c.flags & ~(MOE_FLAG_KEEP_LOGITS | MOE_FLAG_TEST_STALL | MOE_FLAG_RENORM_GATES | MOE_FLAG_TRAINING))
     return fail(MOE_ERR_INVALID_ARG, "unknown flags");
   const int64_t N = c.T * (int64_t)c.top_k;
   if (N > (int64_t)INT32_MAX / 2 || N * (int64_t)(c.d_model > c.d_expert ? c.d_model : c.d_expert) > ((int64_t)1 << 40))
@@ -191,6 +218,8 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
     return fail(MOE_ERR_UNSUPPORTED, "the tensor-core path needs d_model and d_expert multiples of 64 (use MOE_PATH_SIMT)");
   if ((c.flags & MOE_FLAG_TEST_STALL) && !tc)
     return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_TEST_STALL applies to the tensor-core path only");
+  if ((c.flags & MOE_FLAG_TRAINING) && (!tc || c.out_dtype != MOE_BF16))
+    return fail(MOE_ERR_UNSUPPORTED, "MOE_FLAG_TRAINING needs the tensor-core path (bf16 inputs) and bf16 output");
 
   moe_plan_s* p = new (std::nothrow) moe_plan_s();
   if (!p) return fail(MOE_ERR_INTERNAL, "out of host memory");
@@ -207,6 +236,7 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
   s.has_bias = c.has_router_bias;
   s.keep_logits = (c.flags & MOE_FLAG_KEEP_LOGITS) ? 1 : 0;
   s.renorm = (c.flags & MOE_FLAG_RENORM_GATES) ? 1 : 0;
+  s.training = (c.flags & MOE_FLAG_TRAINING) ? 1 : 0;
   s.act_bf16 = bf16 ? 1 : 0;
   s.out_bf16 = c.out_dtype == MOE_BF16 ? 1 : 0;
   // groups of up to kGroupM m-tiles per expert: sum_e ceil(mt_e / G) <= MT / G + E and
@@ -325,6 +355,46 @@ moe_status moe_forward_host(moe_plan_t plan, const void* x_host, void* x_dev, co
     return st;
   e = cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, cs);
   if (e != cudaSuccess) return cuda_fail(e, "copying y to the host");
+  return MOE_OK;
+}
+
+moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
+                        const void* w1, const void* w3, const void* w2, const void* dy, float aux_weight, float* dx,
+                        float* dw_router, float* dbias, float* dw1, float* dw3, float* dw2, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  moe_status st =
+      check_forward_args(plan, x, w_router, router_bias, w1, w3, w2, const_cast<void*>(dy), workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (!plan->shape.training) return fail(MOE_ERR_INVALID_ARG, "moe_backward needs a plan made with MOE_FLAG_TRAINING");
+  const void* outs[] = {dx, dw_router, dw1, dw3, dw2};
+  for (const void* o : outs)
+    if (!o || !aligned(o, 16)) return fail(MOE_ERR_INVALID_ARG, "gradient outputs must be 16-byte aligned device pointers");
+  if (plan->shape.has_bias && dbias && !aligned(dbias, 16)) return fail(MOE_ERR_INVALID_ARG, "dbias must be 16-byte aligned");
+  if ((st = bind_device(plan)) != MOE_OK) return st;
+  const moe::Shape& s = plan->shape;
+  const moe::Ws ws = moe::ws_bind(s, workspace);
+  const moe::Weights w{x, w_router, plan->shape.has_bias ? router_bias : nullptr, w1, w3, w2, nullptr};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int nt_dh = (s.F + 255) / 256;
+  cudaError_t e;
+  if ((e = moe::launch_gather_dy(s, ws, dy, plan->num_sms, false, cs)) != cudaSuccess) return cuda_fail(e, "gather_dy");
+  if ((e = moe::launch_gemm_bwd(moe::kBwdDH, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, true, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "backward GEMM dH");
+  if ((e = moe::launch_gemm_bwd(moe::kBwdDX, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, true, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "backward GEMM dX");
+  if ((e = moe::launch_gemm_bwd(moe::kBwdDW13, s, ws, w, dw1, dw3, plan->num_sms, plan->timeout_ns, true, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "backward GEMM dW1/dW3");
+  if ((e = moe::launch_gemm_bwd(moe::kBwdDW2, s, ws, w, dw2, nullptr, plan->num_sms, plan->timeout_ns, true, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "backward GEMM dW2");
+  if ((e = moe::launch_router_bwd(s, ws, aux_weight, nt_dh, true, cs)) != cudaSuccess) return cuda_fail(e, "router backward");
+  if ((e = moe::launch_dx(s, ws, w_router, dx, true, cs)) != cudaSuccess) return cuda_fail(e, "dx");
+  if ((e = moe::launch_dwr(s, ws, x, ws.dwr_part, ws.dwr_part_b, dw_router, plan->shape.has_bias ? dbias : nullptr,
+                           plan->num_sms, true, cs)) != cudaSuccess)
+    return cuda_fail(e, "router weight gradient");
   return MOE_OK;
 }
 

@@ -1,0 +1,476 @@
+// gemm_bwd.cu -- the grouped GEMMs of the backward pass on the tensor cores (tcgen05, one CTA
+// per 128 x 256 tile, TMA-fed, accumulators in TMEM).
+//
+// Backward of "Distributed Training Part 4 ... MoE + Expert Parallelism" (jesamkim
+// ai-tech-blog) §3 (SwiGLU experts, gate-weighted sum) and §4 (combine / dispatch reversed):
+// for each routed row p of expert e (token t = perm_src[p], gate g = gate_perm[p]):
+//   kDH   dH'[p, f] = sum_c dy[t, c] W2_e[c, f]               (A = dYp  K-major, B = W2 MN-major)
+//         epilogue:  dg partial = sum_f h[p,f] dH'[p,f];  da = g dH' b silu'(a),  db = g dH' silu(a)
+//   kDX   dXslot[slot(p), c] = sum_f da[p,f] W1_e[f,c] + db[p,f] W3_e[f,c]
+//                                                          (A = [da|db] K-major, B = W1|W3 MN-major)
+//   kDW13 [dW1_e; dW3_e][m, c] = sum_{p in e} [da|db][p, m] Xp[p, c]   (both operands MN-major)
+//   kDW2  dW2_e[c, f]          = sum_{p in e} g dy[t, c] h[p, f]       (both operands MN-major)
+// kDH and kDX are grouped over M (the expert's rows, the forward's tile table); kDW13 and
+// kDW2 over K (the expert's rows are the reduction: its last 64-row K block is cut at the
+// expert's end by zeroing the A rows past it in shared memory before the MMA reads them).
+//
+// MN-major operand tiles: TMA boxes of 64 (MN, contiguous) x 64 (K rows) with 128-byte
+// swizzling, side by side 8 KB apart; the descriptor's leading offset is that 8 KB step
+// between 64-wide MN blocks, the stride offset 1 KB between 8-row K groups, and one K=16
+// MMA step is 2 KB.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "gemm_tc.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kTM = 128;  // tile rows (M)
+constexpr int kTN = 256;  // tile columns (N)
+constexpr int kABytes = kTM * kBK * 2;
+constexpr int kBBytes = kTN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBoxBytes = 64 * kBK * 2;  // one 64 x 64 MN-major box
+constexpr int kThreads = 256;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiThreads = 128;
+
+struct Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl);
+
+__host__ __device__ constexpr bool a_mn(int kind) { return kind == kBwdDW13 || kind == kBwdDW2; }
+__host__ __device__ constexpr bool k_grouped(int kind) { return kind == kBwdDW13 || kind == kBwdDW2; }
+
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kBoxBytes >> 4) << 16;  // leading: next 64-wide MN block
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride: next 8 K rows
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack8(uint4 raw, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
+// Work item of one tile.
+struct BTile {
+  int e;
+  int row0, rows;   // M-grouped: routed rows; K-grouped: output rows m0.. (rows = valid)
+  int n_idx;
+  int k_row0;       // K-grouped: first routed row of the expert (the K range)
+  int kblocks;
+  int k_tail;       // valid rows of the last K block (1..64), K-grouped only
+};
+
+struct BwdArgs {
+  Shape s;
+  Ws ws;
+  float* dw_a;      // kDW13: dW1 [E,F,d]; kDW2: dW2 [E,d,F]
+  float* dw_b;      // kDW13: dW3
+};
+
+template <int kKind>
+__device__ __forceinline__ void kind_dims(const Shape& s, int& M, int& N, int& K) {
+  if (kKind == kBwdDH) { M = 0; N = s.F; K = s.d; }
+  if (kKind == kBwdDX) { M = 0; N = s.d; K = 2 * s.F; }
+  if (kKind == kBwdDW13) { M = 2 * s.F; N = s.d; K = 0; }
+  if (kKind == kBwdDW2) { M = s.d; N = s.F; K = 0; }
+}
+
+template <int kKind>
+__device__ __forceinline__ BTile decode(const BwdArgs& a, int tile, int ngroups, int n_tiles, int m_tiles) {
+  BTile b{};
+  if (!k_grouped(kKind)) {
+    const TileInfo ti = decode_tile(a.ws, ngroups, n_tiles, tile);
+    int M, N, K;
+    kind_dims<kKind>(a.s, M, N, K);
+    b.e = ti.e;
+    b.row0 = ti.row0;
+    b.rows = ti.rows;
+    b.n_idx = ti.n_idx;
+    b.kblocks = K / kBK;
+    b.k_tail = kBK;
+    b.k_row0 = 0;
+  } else {
+    int M, N, K;
+    kind_dims<kKind>(a.s, M, N, K);
+    const int per_e = m_tiles * n_tiles;
+    b.e = tile / per_e;
+    const int local = tile % per_e;
+    b.n_idx = local / m_tiles;
+    const int m_idx = local % m_tiles;
+    b.row0 = m_idx * kTM;
+    b.rows = M - b.row0 < kTM ? M - b.row0 : kTM;
+    const int cnt = __ldg(&a.ws.counts[b.e]);
+    b.k_row0 = __ldg(&a.ws.offsets[b.e]);
+    b.kblocks = (cnt + kBK - 1) / kBK;
+    b.k_tail = cnt - (b.kblocks - 1) * kBK;
+  }
+  return b;
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB2, BwdArgs args, int64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(stages + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Shape& s = args.s;
+  const Ws& ws = args.ws;
+  int M, N, K;
+  kind_dims<kKind>(s, M, N, K);
+  const int n_tiles = (N + kTN - 1) / kTN;
+  const int m_tiles = (M + kTM - 1) / kTM;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->tfull[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->tempty[i]), kEpiThreads);
+    }
+    ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int ngroups = (int)ws.hdr[kHdrNumGroups];
+  const int total = k_grouped(kKind) ? s.E * m_tiles * n_tiles : (int)ws.hdr[kHdrNumMTiles] * n_tiles;
+  uint32_t issued = 0, issued_phase = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+        const int n0 = bt.n_idx * kTN;
+        for (int kb = 0; kb < bt.kblocks; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = ptx::smem_u32(&ctl->full[stage]);
+          const uint32_t sa = ptx::smem_u32(stages + (size_t)stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          ptx::mbar_arrive_expect_tx(bar, kStageBytes);
+          if (!a_mn(kKind)) {
+            ptx::tma_load_2d(sa, &tmA, kb * kBK, bt.row0, bar);  // [rows, K]: one 128-row box
+          } else {
+            const int krow = bt.k_row0 + kb * kBK;
+            ptx::tma_load_2d(sa, &tmA, bt.row0, krow, bar);
+            ptx::tma_load_2d(sa + kBoxBytes, &tmA, bt.row0 + 64, krow, bar);
+          }
+          // B: four MN-major boxes of 64 columns
+          const CUtensorMap* bm = &tmB;
+          int brow;
+          if (kKind == kBwdDH) {
+            brow = bt.e * s.d + kb * kBK;
+          } else if (kKind == kBwdDX) {
+            const int fk = s.F / kBK;
+            if (kb >= fk) bm = &tmB2;
+            brow = bt.e * s.F + (kb % fk) * kBK;
+          } else {
+            brow = bt.k_row0 + kb * kBK;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ptx::tma_load_2d(sb + j * kBoxBytes, bm, n0 + 64 * j, brow, bar);
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(ws, MOE_ERR_TIMEOUT, 0x800u + kKind);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer (whole warp:
+    // the lanes zero the rows past an expert's end in its last K block)
+    const uint32_t idesc = ptx::idesc_bf16_f32(kTM, kTN) | (a_mn(kKind) ? (1u << 15) : 0u) | (1u << 16);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+      ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, timeout_ns, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(acc * kTN);
+      for (int kb = 0; kb < bt.kblocks; ++kb) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&ctl->full[stage]), phase, timeout_ns, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        uint8_t* st_base = stages + (size_t)stage * kStageBytes;
+        if (k_grouped(kKind) && kb == bt.kblocks - 1 && bt.k_tail < kBK) {
+          // A is MN-major: K row r of box j is the 128-byte line j*8KB + r*128; zero rows
+          // k_tail..63 of both boxes (whole lines, so the swizzle does not matter)
+          const int lines = kBK - bt.k_tail;
+          for (int i = lane; i < 2 * lines * 8; i += 32) {
+            const int box = i / (lines * 8), rem = i % (lines * 8);
+            const int line = bt.k_tail + rem / 8, chunk = rem % 8;
+            *reinterpret_cast<uint4*>(st_base + box * kBoxBytes + line * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sa = ptx::smem_u32(st_base);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            const uint64_t adesc =
+                a_mn(kKind) ? desc_mnmajor_sw128(sa + ks * 2048) : ptx::desc_kmajor_sw128(sa + ks * 32);
+            ptx::mma_bf16(d_tmem, adesc, desc_mnmajor_sw128(sb + ks * 2048), idesc, (kb | ks) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&ctl->empty[stage]));
+        }
+        __syncwarp();
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::mma_commit(ptx::smem_u32(&ctl->tfull[acc]));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      record_error(ws, MOE_ERR_TIMEOUT, 0x810u + kKind);
+    }
+  } else if (warp >= kEpiWarp0) {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+      ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull[acc]), acc_phase, timeout_ns, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTN);
+      const bool valid = r < bt.rows;
+      const int n0 = bt.n_idx * kTN;
+      if (kKind == kBwdDH) {
+        const int64_t p = (int64_t)bt.row0 + r;
+        const int F = s.F;
+        const float g = valid ? ws.gate_perm[p] : 0.f;
+        const __nv_bfloat16* hrow = reinterpret_cast<const __nv_bfloat16*>(ws.h) + p * F + n0;
+        const __nv_bfloat16* arow = reinterpret_cast<const __nv_bfloat16*>(ws.a1) + p * F + n0;
+        const __nv_bfloat16* brow = reinterpret_cast<const __nv_bfloat16*>(ws.a3) + p * F + n0;
+        __nv_bfloat16* darow = reinterpret_cast<__nv_bfloat16*>(ws.dab) + p * 2 * F + n0;
+        float dg = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kTN; c += 32) {
+          if (n0 + c >= F) break;  // uniform across the warp
+          uint32_t v[32];
+          ptx::tmem_ld_32cols(t_row + c, v);
+          ptx::tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float hv[8], av[8], bv[8];
+              unpack8(*reinterpret_cast<const uint4*>(hrow + c + 8 * u), hv);
+              unpack8(*reinterpret_cast<const uint4*>(arow + c + 8 * u), av);
+              unpack8(*reinterpret_cast<const uint4*>(brow + c + 8 * u), bv);
+              uint4 oa, ob;
+              uint32_t* wa = reinterpret_cast<uint32_t*>(&oa);
+              uint32_t* wb = reinterpret_cast<uint32_t*>(&ob);
+#pragma unroll
+              for (int i = 0; i < 8; i += 2) {
+                float da[2], db[2];
+#pragma unroll
+                for (int z = 0; z < 2; ++z) {
+                  const float dh = __uint_as_float(v[8 * u + i + z]);
+                  dg += hv[i + z] * dh;
+                  const float a = av[i + z];
+                  const float sg = 1.0f / (1.0f + __expf(-a));
+                  da[z] = g * dh * bv[i + z] * sg * (1.0f + a * (1.0f - sg));
+                  db[z] = g * dh * a * sg;
+                }
+                wa[i / 2] = pack2(da[0], da[1]);
+                wb[i / 2] = pack2(db[0], db[1]);
+              }
+              *reinterpret_cast<uint4*>(darow + c + 8 * u) = oa;
+              *reinterpret_cast<uint4*>(darow + F + c + 8 * u) = ob;
+            }
+          }
+        }
+        if (valid) ws.dgp[p * (int64_t)n_tiles + bt.n_idx] = dg;
+      } else if (kKind == kBwdDX) {
+        const int64_t p = (int64_t)bt.row0 + r;
+        int64_t slot = valid ? ws.perm_slot[p] : -1;
+        if (slot >= s.N) slot = -1;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ws.dxslot) + slot * s.d + n0;
+#pragma unroll 1
+        for (int c = 0; c < kTN; c += 32) {
+          if (n0 + c >= s.d) break;
+          uint32_t v[32];
+          ptx::tmem_ld_32cols(t_row + c, v);
+          ptx::tmem_ld_wait();
+          if (slot >= 0) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 o;
+              uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                w[i] = pack2(__uint_as_float(v[8 * u + 2 * i]), __uint_as_float(v[8 * u + 2 * i + 1]));
+              *reinterpret_cast<uint4*>(out + c + 8 * u) = o;
+            }
+          }
+        }
+      } else {
+        // weight gradients, fp32 row-major; an expert without rows gets zeros
+        const int m = bt.row0 + r;
+        float* out;
+        if (kKind == kBwdDW13)
+          out = (m < s.F ? args.dw_a + ((int64_t)bt.e * s.F + m) * s.d : args.dw_b + ((int64_t)bt.e * s.F + (m - s.F)) * s.d) + n0;
+        else
+          out = args.dw_a + ((int64_t)bt.e * s.d + m) * s.F + n0;
+#pragma unroll 1
+        for (int c = 0; c < kTN; c += 32) {
+          if (n0 + c >= N) break;
+          uint32_t v[32];
+          if (bt.kblocks > 0) {
+            ptx::tmem_ld_32cols(t_row + c, v);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (valid) {
+            float4* o4 = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                                  __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&ctl->tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      record_error(ws, MOE_ERR_TIMEOUT, 0x820u + kKind);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0)
+      for (int st = 0; st < kStages; ++st)
+        if (issued & (1u << st))
+          ptx::mbar_wait(ptx::smem_u32(&ctl->full[st]), (issued_phase >> st) & 1u, timeout_ns, nullptr);
+    if (warp == 1 && lane == 0) {
+      ptx::mma_commit(ptx::smem_u32(&ctl->drain));
+      ptx::mbar_wait(ptx::smem_u32(&ctl->drain), 0u, timeout_ns, nullptr);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int kKind>
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const BwdArgs& args,
+                        int num_sms, int64_t timeout_ns, bool pdl, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_bwd_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(gemm_bwd_kernel<kKind>, dim3(num_sms), dim3(kThreads), kSmemBytes, st, pdl, 1, a, b, b2, args,
+                       timeout_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bwd(int kind, const Shape& s, const Ws& ws, const Weights& w, float* dw_a, float* dw_b,
+                            int num_sms, int64_t timeout_ns, bool pdl, cudaStream_t st) {
+  BwdArgs args{s, ws, dw_a, dw_b};
+  CUtensorMap ma, mb, mb2;
+  cudaError_t e;
+  const uint64_t N = (uint64_t)s.N, d = (uint64_t)s.d, F = (uint64_t)s.F, E = (uint64_t)s.E;
+  switch (kind) {
+    case kBwdDH:
+      if ((e = make_tmap_bf16(&ma, ws.dyp, N, d, 128)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb, w.w2, E * d, F, 64)) != cudaSuccess) return e;
+      return launch_kind<kBwdDH>(ma, mb, mb, args, num_sms, timeout_ns, pdl, st);
+    case kBwdDX:
+      if ((e = make_tmap_bf16(&ma, ws.dab, N, 2 * F, 128)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb, w.w1, E * F, d, 64)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb2, w.w3, E * F, d, 64)) != cudaSuccess) return e;
+      return launch_kind<kBwdDX>(ma, mb, mb2, args, num_sms, timeout_ns, pdl, st);
+    case kBwdDW13:
+      if ((e = make_tmap_bf16(&ma, ws.dab, N, 2 * F, 64)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb, ws.xp, N, d, 64)) != cudaSuccess) return e;
+      return launch_kind<kBwdDW13>(ma, mb, mb, args, num_sms, timeout_ns, pdl, st);
+    case kBwdDW2:
+      if ((e = make_tmap_bf16(&ma, ws.dop, N, d, 64)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb, ws.h, N, F, 64)) != cudaSuccess) return e;
+      return launch_kind<kBwdDW2>(ma, mb, mb, args, num_sms, timeout_ns, pdl, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -245,6 +245,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               dst[v] = o;
             }
+            if (s.training) {  // keep W1.x and W3.x of the row for the backward
+              uint4* da1 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.a1) + p * s.F + n0 + c);
+              uint4* da3 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.a3) + p * s.F + n0 + c);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 o1, o3;
+                uint32_t* w1p = reinterpret_cast<uint32_t*>(&o1);
+                uint32_t* w3p = reinterpret_cast<uint32_t*>(&o3);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int i = v * 8 + u * 2;
+                  w1p[u] = pack_bf16x2(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+                  w3p[u] = pack_bf16x2(__uint_as_float(g[i]), __uint_as_float(g[i + 1]));
+                }
+                da1[v] = o1;
+                da3[v] = o3;
+              }
+            }
           }
         }
       } else {

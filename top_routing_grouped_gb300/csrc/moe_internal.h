@@ -26,6 +26,7 @@ struct Shape {
   int has_bias;
   int keep_logits;
   int renorm;     // gates renormalised over the k chosen
+  int training;   // the forward keeps what the backward needs (pre-activations, softmax)
   int act_bf16;   // x and weights are bf16 (else fp32)
   int out_bf16;   // y is bf16 (else fp32)
   int max_groups; // capacity of the group table
@@ -55,13 +56,25 @@ struct Ws {
   void* xp;             // [N, d]
   void* h;              // [N, F]
   void* yslot;          // [N, d]
+  // training (forward keeps, backward uses)
+  void* a1;             // [N, F] bf16: W1_e . x of each routed row
+  void* a3;             // [N, F] bf16: W3_e . x
+  float* probs;         // [T, E] router softmax
+  void* dyp;            // [N, d] bf16: dy of each routed row
+  void* dop;            // [N, d] bf16: gate * dy
+  void* dab;            // [N, 2F] bf16: [dA | dB], gradients of the two pre-activations
+  float* dgp;           // [N, ceil(F/256)] partial dy . o per 256-column tile
+  void* dxslot;         // [N, d] bf16: expert-input gradient of each routed slot (token order)
+  float* dlogit;        // [T, E]
+  float* dwr_part;      // [ceil(T/256), E, d] router-weight gradient partials
+  float* dwr_part_b;    // [ceil(T/256), E]
 };
 
 // Fixed layout of one workspace: byte offsets of each region.
 struct WsLayout {
   size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
       grp_expert, grp_mtile0, grp_mpre, grp_ppre, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
-      yslot, total;
+      yslot, a1, a3, probs, dyp, dop, dab, dgp, dxslot, dlogit, dwr_part, dwr_part_b, total;
 };
 
 WsLayout ws_layout(const Shape& s);
@@ -114,6 +127,13 @@ cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int n
 cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
+
+cudaError_t launch_gather_dy(const Shape& s, const Ws& ws, const void* dy, int num_sms, bool pdl, cudaStream_t st);
+cudaError_t launch_router_bwd(const Shape& s, const Ws& ws, float alpha, int n_tiles_dh, bool pdl, cudaStream_t st);
+cudaError_t launch_dx(const Shape& s, const Ws& ws, const void* w_router, float* dx, bool pdl, cudaStream_t st);
+cudaError_t launch_dwr(const Shape& s, const Ws& ws, const void* x, float* part, float* part_b, float* dwr, float* dbias,
+                       int num_sms, bool pdl, cudaStream_t st);
+int dwr_chunks(const Shape& s);
 
 // Plan internals for entry points defined outside api.cu.
 const Shape* plan_shape(moe_plan_t plan);

@@ -84,7 +84,10 @@ __device__ __forceinline__ void route_finish(const Shape& s, const Ws& ws, int b
       zr[e] = q;
       sum += q;
     }
-    for (int e = 0; e < E; ++e) zr[e] = zr[e] / sum;
+    for (int e = 0; e < E; ++e) {
+      zr[e] = zr[e] / sum;
+      if (s.training) ws.probs[t * E + e] = zr[e];
+    }
     float chosen = 1.f;  // sum of the chosen entries, in slot order (renormalised variant)
     if (s.renorm) {
       chosen = 0.f;

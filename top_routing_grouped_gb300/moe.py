@@ -17,7 +17,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT,
 MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_SIMT, MOE_PATH_TC_1SM = 0, 1, 2
 _PATHS = {"auto": MOE_PATH_AUTO, "simt": MOE_PATH_SIMT, "tc1": MOE_PATH_TC_1SM}
-MOE_FLAG_KEEP_LOGITS, MOE_FLAG_TEST_STALL, MOE_FLAG_RENORM_GATES = 1, 2, 4
+MOE_FLAG_KEEP_LOGITS, MOE_FLAG_TEST_STALL, MOE_FLAG_RENORM_GATES, MOE_FLAG_TRAINING = 1, 2, 4, 8
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -61,6 +61,8 @@ _lib.moe_get_device_status.argtypes = [_P, _P, _P]
 _lib.moe_get_device_status.restype = ctypes.c_int
 _lib.moe_status_string.argtypes = [ctypes.c_int]
 _lib.moe_status_string.restype = ctypes.c_char_p
+_lib.moe_backward.argtypes = [_P] * 8 + [ctypes.c_float] + [_P] * 7 + [ctypes.c_size_t, _P]
+_lib.moe_backward.restype = ctypes.c_int
 _lib.moe_route_noalloc.argtypes = [_P] * 8 + [_P]
 _lib.moe_route_noalloc.restype = ctypes.c_int
 _lib.moe_last_error.argtypes = []
@@ -102,11 +104,12 @@ class MoEPlan:
     top-k, F = d_expert, router temperature tau)."""
 
     def __init__(self, T, d, E, k, F, dtype="bf16", out_dtype=None, tau=1.0, has_bias=False,
-                 path="auto", keep_logits=False, test_stall=False, wait_timeout_ns=0, renorm_gates=False):
+                 path="auto", keep_logits=False, test_stall=False, wait_timeout_ns=0, renorm_gates=False,
+                 training=False):
         act = MOE_BF16 if dtype == "bf16" else MOE_F32
         out = act if out_dtype is None else (MOE_BF16 if out_dtype == "bf16" else MOE_F32)
         flags = ((MOE_FLAG_KEEP_LOGITS if keep_logits else 0) | (MOE_FLAG_TEST_STALL if test_stall else 0)
-                 | (MOE_FLAG_RENORM_GATES if renorm_gates else 0))
+                 | (MOE_FLAG_RENORM_GATES if renorm_gates else 0) | (MOE_FLAG_TRAINING if training else 0))
         self.renorm_gates = bool(renorm_gates)
         self.cfg = MoeConfig(int(T), int(d), int(E), int(k), int(F), act, out, float(tau),
                              1 if has_bias else 0, _PATHS[path],
@@ -153,6 +156,14 @@ class MoEPlan:
         _check(_lib.moe_forward_host(self._h, _ptr(x_host), _ptr(x_dev), _ptr(w_router), _ptr(bias), _ptr(w1),
                                      _ptr(w3), _ptr(w2), _ptr(y_dev), _ptr(y_host), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "moe_forward_host")
+
+    def backward(self, x, w_router, bias, w1, w3, w2, dy, aux_weight, dx, dw_router, dbias, dw1, dw3, dw2, workspace,
+                 stream=None):
+        """Gradients of sum(dy * y) + aux_weight * aux into the given fp32 tensors (needs a
+        training plan and the workspace of its last forward)."""
+        _check(_lib.moe_backward(self._h, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(dy),
+                                 float(aux_weight), _ptr(dx), _ptr(dw_router), _ptr(dbias), _ptr(dw1), _ptr(dw3),
+                                 _ptr(dw2), _ptr(workspace), workspace.numel(), _stream(stream)), "moe_backward")
 
     def aux_loss(self, workspace, out=None, stream=None):
         if out is None:

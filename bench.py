@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", choices=["granularity"], default=None,
                     help="granularity sweep at equal active FLOPs (one JSON line with every G)")
+    ap.add_argument("--train", action="store_true",
+                    help="time the training step: forward (keeping activations) + backward")
     ap.add_argument("--perf-model", action="store_true",
                     help="fit the operator-level model on the listed workloads, predict the sweep")
     return ap.parse_args()
@@ -288,6 +290,68 @@ def run_perf_model(args):
                       "rows": report}), flush=True)
 
 
+def run_train(args):
+    """Forward (training mode) + backward of the workload: one JSON line."""
+    import torch
+    from top_routing_grouped_gb300 import moe
+    from top_routing_grouped_gb300.workloads import SHAPES, make_inputs
+    shape = SHAPES[args.workload]
+    if args.tokens:
+        shape = shape.with_(T=args.tokens)
+    inputs = make_inputs(shape, seed=0)
+    dev = inputs.to("cuda")
+    plan = moe.MoEPlan.for_shape(shape, training=True)
+    ws = plan.new_workspace()
+    y = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
+    g = torch.Generator().manual_seed(1)
+    dy = torch.randn(shape.T, shape.d, generator=g).to(torch.bfloat16).to("cuda")
+    f32 = lambda *sz: torch.empty(*sz, dtype=torch.float32, device="cuda")
+    E, d, F, T = shape.E, shape.d, shape.F, shape.T
+    grads = (f32(T, d), f32(E, d), f32(E) if dev.bias is not None else None, f32(E, F, d), f32(E, F, d), f32(E, d, F))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    fa = (dev.x, dev.w_router, dev.bias, dev.w1, dev.w3, dev.w2, y, ws)
+    ba = lambda: (dev.x, dev.w_router, dev.bias, dev.w1, dev.w3, dev.w2, dy, 0.01) + grads + (ws,)
+    names = plan.backward_stage_names
+    for _ in range(args.warmup):
+        plan.forward(*fa)
+        for i in range(len(names)):
+            plan.backward_stage(i, *ba())
+    K = max(10, args.steps // 5)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record()
+            plan.forward(*fa)
+            for i in range(len(names)):
+                ev[k][i + 1].record()
+                plan.backward_stage(i, *ba())
+            ev[k][len(names) + 1].record()
+        torch.cuda.synchronize()
+    if plan.device_status(ws) != 0:
+        raise RuntimeError("device status error in the training step")
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    st_ms = {n: sum(e[i + 1].elapsed_time(e[i + 2]) for e in ev) / K for i, n in enumerate(names)}
+    bwd_ms = sum(st_ms.values())
+    N = shape.N
+    gemm_flops = {"bwd_dh_swiglu": 2 * N * d * F, "bwd_dx_gemm": 4 * N * d * F, "bwd_dw13": 4 * N * d * F,
+                  "bwd_dw2": 2 * N * d * F}
+    pk = peaks()
+    g_ms = sum(st_ms[n] for n in gemm_flops)
+    g_tf = sum(gemm_flops.values()) / (g_ms / 1e3) / 1e12
+    top = max(gemm_flops, key=lambda n: st_ms[n])
+    top_tf = gemm_flops[top] / (st_ms[top] / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "MoE training step (forward + backward) tokens/s; backward grouped-GEMM TFLOP/s", "unit": "tokens/s",
+        "value": T / ((fwd_ms + bwd_ms) / 1e3), "ms_per_step": fwd_ms + bwd_ms, "forward_ms": fwd_ms, "backward_ms": bwd_ms,
+        "steps": K, "warmup": args.warmup, "config": workload_config(shape, 1), "dtype": "bf16",
+        "backward_stage_ms": st_ms, "backward_gemm_tflops": g_tf, "backward_gemm_frac_of_bf16_peak": g_tf / pk["bf16"],
+        "roofline": {"kernel": top, "bound": "tensor", "achieved": top_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": top_tf / pk["bf16"], "peak_source": f"{pk['src']} bf16 burst"},
+        "clocks": clk.summary()}), flush=True)
+
+
 def run_reference(args):
     """--impl reference: the oracle on the host cores, rank 0 only."""
     rank = int(os.environ.get("RANK", "0"))
@@ -336,6 +400,8 @@ def main():
         return run_sweep(args)
     if args.perf_model:
         return run_perf_model(args)
+    if args.train:
+        return run_train(args)
 
     import torch
     import torch.distributed as dist

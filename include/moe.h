@@ -160,6 +160,15 @@ moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, co
                         float* dw_router, float* dbias, float* dw1, float* dw3, float* dw2, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Number and names of the kernel stages moe_backward enqueues, and one stage alone (same
+ * arguments; stages 0..n-1 in order on one stream are exactly moe_backward). */
+int32_t moe_backward_stage_count(moe_plan_t plan);
+const char* moe_backward_stage_name(moe_plan_t plan, int32_t stage);
+moe_status moe_backward_stage(moe_plan_t plan, int32_t stage, const void* x, const void* w_router,
+                              const float* router_bias, const void* w1, const void* w3, const void* w2, const void* dy,
+                              float aux_weight, float* dx, float* dw_router, float* dbias, float* dw1, float* dw3,
+                              float* dw2, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Copy the balancing scalar aux = E * sum_e f_e P_e of the last forward on `workspace`
  * to the device float *aux_out (stream-ordered, asynchronous).  (§3 Load-Balancing Loss) */
 moe_status moe_aux_loss(moe_plan_t plan, const void* workspace, float* aux_out, void* stream);

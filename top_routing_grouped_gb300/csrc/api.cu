@@ -104,7 +104,7 @@ WsLayout ws_layout(const Shape& s) {
   L.h = take(N * (size_t)s.F * esz);
   L.yslot = take(N * (size_t)s.d * esz);
   if (s.training) {
-    const size_t nt = ((size_t)s.F + 255) / 256, chunks = ((size_t)s.T + 255) / 256;
+    const size_t nt = 2 * (((size_t)s.F + 255) / 256), chunks = (size_t)dwr_chunks(s);
     L.a1 = take(N * (size_t)s.F * 2);
     L.a3 = take(N * (size_t)s.F * 2);
     L.probs = take((size_t)s.T * E * 4);
@@ -358,10 +358,21 @@ moe_status moe_forward_host(moe_plan_t plan, const void* x_host, void* x_dev, co
   return MOE_OK;
 }
 
-moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
-                        const void* w1, const void* w3, const void* w2, const void* dy, float aux_weight, float* dx,
-                        float* dw_router, float* dbias, float* dw1, float* dw3, float* dw2, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+static constexpr const char* kBwdStageNames[] = {"gather_dy", "bwd_dh_swiglu", "bwd_dx_gemm", "bwd_dw13", "bwd_dw2",
+                                                  "router_bwd", "bwd_dx_combine", "bwd_dw_router"};
+static constexpr int kNumBwdStages = 8;
+
+int32_t moe_backward_stage_count(moe_plan_t plan) { return plan ? kNumBwdStages : 0; }
+
+const char* moe_backward_stage_name(moe_plan_t plan, int32_t stage) {
+  if (!plan || stage < 0 || stage >= kNumBwdStages) return nullptr;
+  return kBwdStageNames[stage];
+}
+
+moe_status moe_backward_stage(moe_plan_t plan, int32_t stage, const void* x, const void* w_router,
+                              const float* router_bias, const void* w1, const void* w3, const void* w2, const void* dy,
+                              float aux_weight, float* dx, float* dw_router, float* dbias, float* dw1, float* dw3,
+                              float* dw2, void* workspace, size_t workspace_bytes, void* stream) {
   moe_status st =
       check_forward_args(plan, x, w_router, router_bias, w1, w3, w2, const_cast<void*>(dy), workspace, workspace_bytes);
   if (st != MOE_OK) return st;
@@ -370,31 +381,44 @@ moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, co
   for (const void* o : outs)
     if (!o || !aligned(o, 16)) return fail(MOE_ERR_INVALID_ARG, "gradient outputs must be 16-byte aligned device pointers");
   if (plan->shape.has_bias && dbias && !aligned(dbias, 16)) return fail(MOE_ERR_INVALID_ARG, "dbias must be 16-byte aligned");
+  if (stage < 0 || stage >= kNumBwdStages) return fail(MOE_ERR_INVALID_ARG, "backward stage %d out of range", stage);
   if ((st = bind_device(plan)) != MOE_OK) return st;
   const moe::Shape& s = plan->shape;
   const moe::Ws ws = moe::ws_bind(s, workspace);
   const moe::Weights w{x, w_router, plan->shape.has_bias ? router_bias : nullptr, w1, w3, w2, nullptr};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const int nt_dh = (s.F + 255) / 256;
-  cudaError_t e;
-  if ((e = moe::launch_gather_dy(s, ws, dy, plan->num_sms, false, cs)) != cudaSuccess) return cuda_fail(e, "gather_dy");
-  if ((e = moe::launch_gemm_bwd(moe::kBwdDH, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, true, cs)) !=
-      cudaSuccess)
-    return cuda_fail(e, "backward GEMM dH");
-  if ((e = moe::launch_gemm_bwd(moe::kBwdDX, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, true, cs)) !=
-      cudaSuccess)
-    return cuda_fail(e, "backward GEMM dX");
-  if ((e = moe::launch_gemm_bwd(moe::kBwdDW13, s, ws, w, dw1, dw3, plan->num_sms, plan->timeout_ns, true, cs)) !=
-      cudaSuccess)
-    return cuda_fail(e, "backward GEMM dW1/dW3");
-  if ((e = moe::launch_gemm_bwd(moe::kBwdDW2, s, ws, w, dw2, nullptr, plan->num_sms, plan->timeout_ns, true, cs)) !=
-      cudaSuccess)
-    return cuda_fail(e, "backward GEMM dW2");
-  if ((e = moe::launch_router_bwd(s, ws, aux_weight, nt_dh, true, cs)) != cudaSuccess) return cuda_fail(e, "router backward");
-  if ((e = moe::launch_dx(s, ws, w_router, dx, true, cs)) != cudaSuccess) return cuda_fail(e, "dx");
-  if ((e = moe::launch_dwr(s, ws, x, ws.dwr_part, ws.dwr_part_b, dw_router, plan->shape.has_bias ? dbias : nullptr,
-                           plan->num_sms, true, cs)) != cudaSuccess)
-    return cuda_fail(e, "router weight gradient");
+  const bool pdl = stage > 0;  // chained to the previous backward kernel
+  cudaError_t e = cudaSuccess;
+  switch (stage) {
+    case 0: e = moe::launch_gather_dy(s, ws, dy, plan->num_sms, false, cs); break;
+    case 1: e = moe::launch_gemm_bwd(moe::kBwdDH, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
+    case 2: e = moe::launch_gemm_bwd(moe::kBwdDX, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
+    case 3: e = moe::launch_gemm_bwd(moe::kBwdDW13, s, ws, w, dw1, dw3, plan->num_sms, plan->timeout_ns, pdl, cs); break;
+    case 4: e = moe::launch_gemm_bwd(moe::kBwdDW2, s, ws, w, dw2, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
+    case 5: e = moe::launch_router_bwd(s, ws, aux_weight, 2 * ((s.F + 255) / 256), pdl, cs); break;
+    case 6: e = moe::launch_dx(s, ws, w_router, dx, pdl, cs); break;
+    case 7:
+      e = moe::launch_dwr(s, ws, x, ws.dwr_part, ws.dwr_part_b, dw_router, plan->shape.has_bias ? dbias : nullptr,
+                          plan->num_sms, pdl, cs);
+      break;
+  }
+  if (e != cudaSuccess) {
+    char what[64];
+    snprintf(what, sizeof what, "launching backward stage %s", kBwdStageNames[stage]);
+    return cuda_fail(e, what);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
+                        const void* w1, const void* w3, const void* w2, const void* dy, float aux_weight, float* dx,
+                        float* dw_router, float* dbias, float* dw1, float* dw3, float* dw2, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  for (int i = 0; i < kNumBwdStages; ++i) {
+    moe_status st = moe_backward_stage(plan, i, x, w_router, router_bias, w1, w3, w2, dy, aux_weight, dx, dw_router,
+                                       dbias, dw1, dw3, dw2, workspace, workspace_bytes, stream);
+    if (st != MOE_OK) return st;
+  }
   return MOE_OK;
 }
 

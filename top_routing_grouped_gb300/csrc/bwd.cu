@@ -117,107 +117,125 @@ __global__ void __launch_bounds__(128) router_bwd_kernel(Shape s, Ws ws, float a
   for (int e = 0; e < E; ++e) ws.dlogit[t * E + e] = pt[e] * (dp[e] - pdp) / s.tau;
 }
 
-// dx[t, c] = sum_j dXslot[t k + j, c] + sum_e dlogit[t, e] W_r[e, c].  Tiles of 32 tokens x
-// 128 columns; dlogit and W_r staged in shared memory over E in chunks of 32.
-constexpr int kDxT = 32, kDxC = 128, kDxE = 32;
+// dx[t, c] = sum_j dXslot[t k + j, c] + sum_e dlogit[t, e] W_r[e, c].  Tiles of 64 tokens x
+// 128 columns, 256 threads each holding 4 tokens x 8 columns in registers; dlogit and W_r
+// staged in shared memory over E in chunks of 32.
+constexpr int kDxT = 64, kDxC = 128, kDxE = 32;
 __global__ void __launch_bounds__(256) dx_kernel(Shape s, Ws ws, const void* w_router, float* dx) {
-  __shared__ float zl[kDxT][kDxE + 1];
-  __shared__ float wr[kDxE][kDxC + 1];
+  __shared__ float zl[kDxE][kDxT + 4];  // transposed: zl[e][t]
+  __shared__ float wr[kDxE][kDxC + 4];
   const int tid = threadIdx.x;
-  const int c_local = tid % kDxC;        // column of this thread
-  const int t_half = tid / kDxC;         // 0/1: tokens t_half, t_half+2, ...
+  const int tg = tid / 16, cg = tid % 16;  // tokens tg*4.., columns cg*8..
   const int64_t t0 = (int64_t)blockIdx.y * kDxT;
   const int c0 = blockIdx.x * kDxC;
   pdl_wait();
   pdl_launch_dependents();
-  float acc[kDxT / 2];
+  float acc[4][8];
 #pragma unroll
-  for (int i = 0; i < kDxT / 2; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
   for (int e0 = 0; e0 < s.E; e0 += kDxE) {
     for (int i = tid; i < kDxT * kDxE; i += 256) {
       const int tt = i / kDxE, ee = i % kDxE;
       const int64_t t = t0 + tt;
-      zl[tt][ee] = (t < s.T && e0 + ee < s.E) ? ws.dlogit[t * s.E + e0 + ee] : 0.f;
+      zl[ee][tt] = (t < s.T && e0 + ee < s.E) ? ws.dlogit[t * s.E + e0 + ee] : 0.f;
     }
     for (int i = tid; i < kDxE * kDxC; i += 256) {
       const int ee = i / kDxC, cc = i % kDxC;
       wr[ee][cc] = (e0 + ee < s.E && c0 + cc < s.d) ? load_act(w_router, 1, (int64_t)(e0 + ee) * s.d + c0 + cc) : 0.f;
     }
     __syncthreads();
+#pragma unroll 4
+    for (int ee = 0; ee < kDxE; ++ee) {
+      const float4 za = *reinterpret_cast<const float4*>(&zl[ee][tg * 4]);
+      const float4 w0 = *reinterpret_cast<const float4*>(&wr[ee][cg * 8]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&wr[ee][cg * 8 + 4]);
+      const float zv[4] = {za.x, za.y, za.z, za.w};
+      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int i = 0; i < kDxT / 2; ++i) {
-      const int tt = t_half + 2 * i;
-      float a = acc[i];
-#pragma unroll 8
-      for (int ee = 0; ee < kDxE; ++ee) a = fmaf(zl[tt][ee], wr[ee][c_local], a);
-      acc[i] = a;
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(zv[i], wv[j], acc[i][j]);
     }
     __syncthreads();
   }
-  const int c = c0 + c_local;
-  if (c >= s.d) return;
 #pragma unroll
-  for (int i = 0; i < kDxT / 2; ++i) {
-    const int64_t t = t0 + t_half + 2 * i;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t t = t0 + tg * 4 + i;
     if (t >= s.T) continue;
-    float v = acc[i];
-    for (int j = 0; j < s.k; ++j)
-      v += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(ws.dxslot)[(t * s.k + j) * s.d + c]);
-    dx[t * s.d + c] = v;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + cg * 8 + j;
+      if (c >= s.d) continue;
+      float v = acc[i][j];
+      for (int q = 0; q < s.k; ++q)
+        v += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(ws.dxslot)[(t * s.k + q) * s.d + c]);
+      dx[t * s.d + c] = v;
+    }
   }
 }
 
 // Partial router-weight gradients over chunks of kDwrTok tokens: part[chunk][e][c] and
-// part_b[chunk][e]; a second kernel adds the chunks in order.
-constexpr int kDwrTok = 256, kDwrE = 16, kDwrC = 128;
+// part_b[chunk][e] for a tile of 64 experts x 128 columns (each thread 4 experts x 8
+// columns); a second kernel adds the chunks in order.
+constexpr int kDwrTok = 512, kDwrE = 64, kDwrC = 128, kDwrK = 32;
 __global__ void __launch_bounds__(256) dwr_partial_kernel(Shape s, Ws ws, const void* x, float* part, float* part_b) {
-  __shared__ float zl[32][kDwrE + 1];
-  __shared__ float xs[32][kDwrC + 1];
+  __shared__ float zl[kDwrK][kDwrE + 4];
+  __shared__ float xs[kDwrK][kDwrC + 4];
   const int tid = threadIdx.x;
-  const int c_local = tid % kDwrC;
-  const int e_half = tid / kDwrC;  // experts e_half, e_half + 2, ...
+  const int eg = tid / 16, cg = tid % 16;
   const int c0 = blockIdx.x * kDwrC;
   const int e0 = blockIdx.y * kDwrE;
   const int chunk = blockIdx.z;
   const int64_t tbeg = (int64_t)chunk * kDwrTok;
   pdl_wait();
   pdl_launch_dependents();
-  float acc[kDwrE / 2], bacc[kDwrE / 2];
+  float acc[4][8], bacc[4];
 #pragma unroll
-  for (int i = 0; i < kDwrE / 2; ++i) acc[i] = bacc[i] = 0.f;
-  for (int64_t tb = tbeg; tb < tbeg + kDwrTok && tb < s.T; tb += 32) {
-    for (int i = tid; i < 32 * kDwrE; i += 256) {
+  for (int i = 0; i < 4; ++i) {
+    bacc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  }
+  for (int64_t tb = tbeg; tb < tbeg + kDwrTok && tb < s.T; tb += kDwrK) {
+    for (int i = tid; i < kDwrK * kDwrE; i += 256) {
       const int tt = i / kDwrE, ee = i % kDwrE;
       const int64_t t = tb + tt;
       zl[tt][ee] = (t < s.T && e0 + ee < s.E) ? ws.dlogit[t * s.E + e0 + ee] : 0.f;
     }
-    for (int i = tid; i < 32 * kDwrC; i += 256) {
+    for (int i = tid; i < kDwrK * kDwrC; i += 256) {
       const int tt = i / kDwrC, cc = i % kDwrC;
       const int64_t t = tb + tt;
       xs[tt][cc] = (t < s.T && c0 + cc < s.d) ? load_act(x, s.act_bf16, t * s.d + c0 + cc) : 0.f;
     }
     __syncthreads();
+#pragma unroll 4
+    for (int tt = 0; tt < kDwrK; ++tt) {
+      const float4 za = *reinterpret_cast<const float4*>(&zl[tt][eg * 4]);
+      const float4 x0 = *reinterpret_cast<const float4*>(&xs[tt][cg * 8]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&xs[tt][cg * 8 + 4]);
+      const float zv[4] = {za.x, za.y, za.z, za.w};
+      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-    for (int i = 0; i < kDwrE / 2; ++i) {
-      const int ee = e_half + 2 * i;
-      float a = acc[i], b = bacc[i];
-#pragma unroll 8
-      for (int tt = 0; tt < 32; ++tt) {
-        a = fmaf(zl[tt][ee], xs[tt][c_local], a);
-        b += zl[tt][ee];
+      for (int i = 0; i < 4; ++i) {
+        bacc[i] += zv[i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(zv[i], xv[j], acc[i][j]);
       }
-      acc[i] = a;
-      bacc[i] = b;
     }
     __syncthreads();
   }
-  const int c = c0 + c_local;
 #pragma unroll
-  for (int i = 0; i < kDwrE / 2; ++i) {
-    const int e = e0 + e_half + 2 * i;
+  for (int i = 0; i < 4; ++i) {
+    const int e = e0 + eg * 4 + i;
     if (e >= s.E) continue;
-    if (c < s.d) part[((int64_t)chunk * s.E + e) * s.d + c] = acc[i];
-    if (blockIdx.x == 0 && c_local == 0) part_b[(int64_t)chunk * s.E + e] = bacc[i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + cg * 8 + j;
+      if (c < s.d) part[((int64_t)chunk * s.E + e) * s.d + c] = acc[i][j];
+    }
+    if (blockIdx.x == 0 && cg == 0) part_b[(int64_t)chunk * s.E + e] = bacc[i];
   }
 }
 

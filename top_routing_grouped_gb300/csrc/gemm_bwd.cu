@@ -35,9 +35,9 @@ constexpr int kABytes = kTM * kBK * 2;
 constexpr int kBBytes = kTN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBoxBytes = 64 * kBK * 2;  // one 64 x 64 MN-major box
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiThreads = 256;  // 8 warps: two per TMEM lane quarter, one per 128-column half
 
 struct Ctl {
   uint64_t full[kStages];
@@ -293,7 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kEpiWarp0) {
     // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                          // TMEM lane quarter
+    const int half = (warp - kEpiWarp0) >> 2;        // columns [128 half, 128 half + 128)
+    const int c_beg = half * (kTN / 2), c_end = c_beg + kTN / 2;
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* darow = reinterpret_cast<__nv_bfloat16*>(ws.dab) + p * 2 * F + n0;
         float dg = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < kTN; c += 32) {
+        for (int c = c_beg; c < c_end; c += 32) {
           if (n0 + c >= F) break;  // uniform across the warp
           uint32_t v[32];
           ptx::tmem_ld_32cols(t_row + c, v);
@@ -352,14 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (valid) ws.dgp[p * (int64_t)n_tiles + bt.n_idx] = dg;
+        if (valid) ws.dgp[p * (int64_t)(2 * n_tiles) + 2 * bt.n_idx + half] = dg;
       } else if (kKind == kBwdDX) {
         const int64_t p = (int64_t)bt.row0 + r;
         int64_t slot = valid ? ws.perm_slot[p] : -1;
         if (slot >= s.N) slot = -1;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ws.dxslot) + slot * s.d + n0;
 #pragma unroll 1
-        for (int c = 0; c < kTN; c += 32) {
+        for (int c = c_beg; c < c_end; c += 32) {
           if (n0 + c >= s.d) break;
           uint32_t v[32];
           ptx::tmem_ld_32cols(t_row + c, v);
@@ -385,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           out = args.dw_a + ((int64_t)bt.e * s.d + m) * s.F + n0;
 #pragma unroll 1
-        for (int c = 0; c < kTN; c += 32) {
+        for (int c = c_beg; c < c_end; c += 32) {
           if (n0 + c >= N) break;
           uint32_t v[32];
           if (bt.kblocks > 0) {

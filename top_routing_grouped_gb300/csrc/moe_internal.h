@@ -63,7 +63,7 @@ struct Ws {
   void* dyp;            // [N, d] bf16: dy of each routed row
   void* dop;            // [N, d] bf16: gate * dy
   void* dab;            // [N, 2F] bf16: [dA | dB], gradients of the two pre-activations
-  float* dgp;           // [N, ceil(F/256)] partial dy . o per 256-column tile
+  float* dgp;           // [N, 2 ceil(F/256)] partial dy . o per 128-column half tile
   void* dxslot;         // [N, d] bf16: expert-input gradient of each routed slot (token order)
   float* dlogit;        // [T, E]
   float* dwr_part;      // [ceil(T/256), E, d] router-weight gradient partials

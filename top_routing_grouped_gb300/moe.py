@@ -63,6 +63,12 @@ _lib.moe_status_string.argtypes = [ctypes.c_int]
 _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_backward.argtypes = [_P] * 8 + [ctypes.c_float] + [_P] * 7 + [ctypes.c_size_t, _P]
 _lib.moe_backward.restype = ctypes.c_int
+_lib.moe_backward_stage.argtypes = [_P, ctypes.c_int32] + [_P] * 7 + [ctypes.c_float] + [_P] * 7 + [ctypes.c_size_t, _P]
+_lib.moe_backward_stage.restype = ctypes.c_int
+_lib.moe_backward_stage_count.argtypes = [_P]
+_lib.moe_backward_stage_count.restype = ctypes.c_int32
+_lib.moe_backward_stage_name.argtypes = [_P, ctypes.c_int32]
+_lib.moe_backward_stage_name.restype = ctypes.c_char_p
 _lib.moe_route_noalloc.argtypes = [_P] * 8 + [_P]
 _lib.moe_route_noalloc.restype = ctypes.c_int
 _lib.moe_last_error.argtypes = []
@@ -164,6 +170,17 @@ class MoEPlan:
         _check(_lib.moe_backward(self._h, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(dy),
                                  float(aux_weight), _ptr(dx), _ptr(dw_router), _ptr(dbias), _ptr(dw1), _ptr(dw3),
                                  _ptr(dw2), _ptr(workspace), workspace.numel(), _stream(stream)), "moe_backward")
+
+    @property
+    def backward_stage_names(self):
+        return [_lib.moe_backward_stage_name(self._h, i).decode() for i in range(_lib.moe_backward_stage_count(self._h))]
+
+    def backward_stage(self, stage, x, w_router, bias, w1, w3, w2, dy, aux_weight, dx, dw_router, dbias, dw1, dw3, dw2,
+                       workspace, stream=None):
+        _check(_lib.moe_backward_stage(self._h, int(stage), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w1), _ptr(w3),
+                                       _ptr(w2), _ptr(dy), float(aux_weight), _ptr(dx), _ptr(dw_router), _ptr(dbias),
+                                       _ptr(dw1), _ptr(dw3), _ptr(dw2), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "moe_backward_stage")
 
     def aux_loss(self, workspace, out=None, stream=None):
         if out is None:

@@ -19,6 +19,23 @@ __device__ __forceinline__ void store_act(void* base, int bf16, int64_t i, float
     reinterpret_cast<float*>(base)[i] = v;
 }
 
+// Logistic sigmoid through the identity sigmoid(a) = (1 + tanh(a/2)) / 2 with the hardware
+// tanh approximation (relative error about 2^-11): one transcendental and no divide, well
+// below the bf16 rounding the GEMM epilogues apply to their results.
+__device__ __forceinline__ float sigmoid_fast(float a) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * a));
+  return fmaf(0.5f, t, 0.5f);
+}
+
+// SiLU(a) = a * sigmoid(a) = h + h tanh(h), h = a/2.
+__device__ __forceinline__ float silu_fast(float a) {
+  const float h = 0.5f * a;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
+
 // First error wins; `where` records which kernel/site saw it.
 __device__ __forceinline__ void record_error(const Ws& ws, uint32_t code, uint32_t where) {
   if (atomicCAS(&ws.hdr[kHdrStatus], 0u, code) == 0u) ws.hdr[kHdrWhere] = where;

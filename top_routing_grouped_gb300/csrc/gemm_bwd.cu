@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float dh = __uint_as_float(v[8 * u + i + z]);
                   dg += hv[i + z] * dh;
                   const float a = av[i + z];
-                  const float sg = 1.0f / (1.0f + __expf(-a));
+                  const float sg = sigmoid_fast(a);
                   da[z] = g * dh * bv[i + z] * sg * (1.0f + a * (1.0f - sg));
                   db[z] = g * dh * a * sg;
                 }

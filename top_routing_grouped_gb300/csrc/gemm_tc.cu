@@ -67,7 +67,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu(float a) { return a / (1.0f + __expf(-a)); }
+__device__ __forceinline__ float silu(float a) { return silu_fast(a); }
 
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)

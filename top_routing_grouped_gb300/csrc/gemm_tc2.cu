@@ -57,7 +57,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu(float a) { return a / (1.0f + __expf(-a)); }
+__device__ __forceinline__ float silu(float a) { return silu_fast(a); }
 
 __device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
   ctl->abort = 1;

@@ -289,7 +289,8 @@ static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& 
     case 0:
       e = cudaMemsetAsync(ws.hdr, 0, 4 * sizeof(uint32_t), st);
       if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
-      e = plan->tc ? moe::launch_route_tc(s, ws, w, plan->timeout_ns, st) : moe::launch_route_simt(s, ws, w, st);
+      e = plan->tc ? moe::launch_route_tc(s, ws, w, plan->num_sms, plan->timeout_ns, st)
+                   : moe::launch_route_simt(s, ws, w, st);
       break;
     case 1: e = moe::launch_scan(s, ws, pdl, st); break;
     case 2: e = moe::launch_permute(s, ws, w, plan->num_sms, pdl, st); break;

@@ -36,6 +36,24 @@ __device__ __forceinline__ float silu_fast(float a) {
   return fmaf(h, t, h);
 }
 
+// shared-memory loads and stores by shared-window address: the compiler cannot tell a
+// generic pointer into shared memory from a global one, and orders such accesses
+// conservatively; these keep the epilogues' traffic on the shared path, issued in the
+// order written
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float& a, float& b, float& c, float& d) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr));
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // First error wins; `where` records which kernel/site saw it.
 __device__ __forceinline__ void record_error(const Ws& ws, uint32_t code, uint32_t where) {
   if (atomicCAS(&ws.hdr[kHdrStatus], 0u, code) == 0u) ws.hdr[kHdrWhere] = where;

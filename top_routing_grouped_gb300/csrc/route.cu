@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kRouteBlock) route_simt_kernel(Shape s, Ws ws,
   float* z_s = reinterpret_cast<float*>(smem_raw);                  // [128][E+1]
   float* x_s = z_s + kRouteBlock * ldz;                              // [128][33]
   float* w_s = x_s + kRouteBlock * (kRouteChunk + 1);                // [E][33]
-  uint32_t* mask_s = reinterpret_cast<uint32_t*>(w_s + s.E * (kRouteChunk + 1));  // [E][4]
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(w_s + s.E * (kRouteChunk + 1));  // [E][4], then [2][128]
 
   const int r = threadIdx.x;
   const int blk = blockIdx.x;
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kRouteBlock) route_simt_kernel(Shape s, Ws ws,
 size_t route_simt_smem(const Shape& s) {
   return sizeof(float) * ((size_t)kRouteBlock * (s.E + 1) + (size_t)kRouteBlock * (kRouteChunk + 1) +
                           (size_t)s.E * (kRouteChunk + 1)) +
-         sizeof(uint32_t) * 4 * (size_t)s.E;
+         sizeof(uint32_t) * (4 * (size_t)s.E + 2 * kRouteBlock);
 }
 
 cudaError_t launch_route_simt(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st) {

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kRouteBlock) route_noalloc_kernel(Shape s, Ws 
   float* z_s = reinterpret_cast<float*>(smem_raw);                       // [128][E+1]
   float* x_s = z_s + kRouteBlock * ldz;                                   // [128][33]
   float* w_s = x_s + kRouteBlock * (kChunk + 1);                          // [E][33]
-  uint32_t* mask_s = reinterpret_cast<uint32_t*>(w_s + s.E * (kChunk + 1));  // [E][4]
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(w_s + s.E * (kChunk + 1));  // [E][4], then [2][128]
   __shared__ float red[kMaxExperts];
   __shared__ int last;
 
@@ -186,7 +186,7 @@ extern "C" moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const vo
   }
   const size_t smem = sizeof(float) * ((size_t)kRouteBlock * (s.E + 1) + (size_t)kRouteBlock * (kChunk + 1) +
                                        (size_t)s.E * (kChunk + 1)) +
-                      sizeof(uint32_t) * 4 * (size_t)s.E;
+                      sizeof(uint32_t) * (4 * (size_t)s.E + 2 * kRouteBlock);
   if ((e = cudaFuncSetAttribute(route_noalloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) ==
       cudaSuccess) {
     route_noalloc_kernel<<<s.nblk, kRouteBlock, smem, st>>>(s, ws, w, reinterpret_cast<uint32_t*>(base), expert_counts,

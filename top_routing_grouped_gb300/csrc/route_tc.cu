@@ -27,6 +27,14 @@ constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kXBytes = kRouteBlock * kBK * 2;  // 16 KB
+constexpr int kMaxAcc = 4;                       // TMEM accumulators the K loop may use
+
+// z = (x.W_r + b) / tau from the summed dot product (a temperature of 1 divides exactly,
+// so it is skipped)
+__device__ __forceinline__ float finish_logit(float dot, float b, float tau) {
+  const float z = dot + b;
+  return tau == 1.f ? z : z / tau;
+}
 
 struct RouteCtl {
   uint64_t full[kMaxStages];
@@ -39,6 +47,9 @@ struct RouteCtl {
 };
 
 struct RouteGeom {
+  int split;        // CTAs (one cluster) sharing one token block, each on 1/split of d
+  int kb_per;       // 64-column K blocks per CTA
+  int recv_bytes;   // leader's buffer for the other CTAs' partial logits
   int e_pad;        // MMA N: E rounded up to a multiple of 16 (>= 16)
   int n_acc;        // TMEM accumulators the K loop is spread over (summed in fp32 at the end)
   int stages;
@@ -48,30 +59,41 @@ struct RouteGeom {
   size_t smem;      // dynamic shared memory
 };
 
-RouteGeom route_geom(const Shape& s) {
+RouteGeom route_geom(const Shape& s, int num_sms) {
   RouteGeom g;
   g.e_pad = ((s.E + 15) / 16) * 16;
   if (g.e_pad < 16) g.e_pad = 16;
+  const int kblocks = s.d / kBK;
+  // Few token blocks (small T) leave most SMs idle while each CTA streams its x rows with a
+  // few stages in flight: split d over a cluster of up to 4 CTAs; the leader adds the
+  // others' partial logits (in rank order) from its shared memory.
+  g.split = 1;
+  while (g.split < 4 && s.nblk * g.split * 2 <= num_sms && g.split * 2 <= kblocks &&
+         (2 * g.split - 1) * kRouteBlock * (s.E + 1) * 4 <= 64 * 1024)
+    g.split *= 2;
+  g.kb_per = (kblocks + g.split - 1) / g.split;
+  g.recv_bytes = (g.split - 1) * kRouteBlock * (s.E + 1) * 4;
   g.stage_bytes = kXBytes + g.e_pad * kBK * 2;
   // up to ~96 KB of ring so that two CTAs share an SM (more bytes in flight per SM)
   g.stages = (96 * 1024) / g.stage_bytes;
   if (g.stages > kMaxStages) g.stages = kMaxStages;
+  if (g.stages > g.kb_per) g.stages = g.kb_per;
   if (g.stages < 2) g.stages = 2;
-  const int zs = kRouteBlock * (s.E + 1) * 4 + 4 * s.E * 4;
+  const int zs = kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4;  // logits, then route_finish's masks
   g.body_bytes = g.stages * g.stage_bytes > zs ? g.stages * g.stage_bytes : zs;
   g.body_bytes = (g.body_bytes + 1023) / 1024 * 1024;
   // The tensor core's fp32 accumulation chain over K = d loses more than a SIMT sum; K-block
   // kb goes to accumulator kb % n_acc and the epilogue adds the n_acc partial sums in fp32
   // (round to nearest), which keeps the logits within a few 1e-7 relative.
   g.n_acc = 512 / g.e_pad;
-  if (g.n_acc > 4) g.n_acc = 4;
+  if (g.n_acc > kMaxAcc) g.n_acc = kMaxAcc;
   uint32_t c = 32;
   while (c < (uint32_t)(g.e_pad * g.n_acc)) c <<= 1;
   g.tmem_cols = c;
   // more than half of TMEM: make the CTA big enough in shared memory that two never share an
   // SM (the second would only wait in tcgen05.alloc)
   if (g.tmem_cols > 256 && g.body_bytes < 120 * 1024) g.body_bytes = 120 * 1024;
-  g.smem = 1024 + (size_t)g.body_bytes + sizeof(RouteCtl);
+  g.smem = 1024 + (size_t)g.body_bytes + sizeof(RouteCtl) + 16 + (size_t)g.recv_bytes + (size_t)g.e_pad * 4;
   return g;
 }
 
@@ -91,10 +113,16 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* body = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   RouteCtl* ctl = reinterpret_cast<RouteCtl*>(body + g.body_bytes);
+  // the other CTAs' partial logits [split-1][128][E+1], then the router bias [e_pad]
+  // (zero past E; 16-byte aligned, as 128 * 4 divides the first part)
+  float* recv = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(ctl + 1) + 15) & ~uintptr_t(15));
+  float* bias_s = recv + (g.split - 1) * kRouteBlock * (s.E + 1);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int blk = blockIdx.x;
-  const int kblocks = s.d / kBK;
+  const uint32_t rank = g.split > 1 ? ptx::cluster_ctarank() : 0u;
+  const int blk = g.split > 1 ? (int)ptx::cluster_id_x() : (int)blockIdx.x;  // token block
+  const int kb0 = (int)rank * g.kb_per;                                          // this CTA's K range
+  const int kblocks = max(0, min(s.d / kBK, kb0 + g.kb_per) - kb0);  // may be 0 for the last rank
   pdl_launch_dependents();  // the scan may be scheduled; it waits for this grid to finish
 
   if (threadIdx.x == 0) {
@@ -133,8 +161,8 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
         const uint32_t bar = ptx::smem_u32(&ctl->full[stage]);
         const uint32_t sa = ptx::smem_u32(body + (size_t)stage * g.stage_bytes);
         ptx::mbar_arrive_expect_tx(bar, (uint32_t)g.stage_bytes);
-        ptx::tma_load_2d(sa, &tmX, kb * kBK, blk * kRouteBlock, bar);
-        ptx::tma_load_2d(sa + kXBytes, &tmW, kb * kBK, 0, bar);
+        ptx::tma_load_2d(sa, &tmX, (kb0 + kb) * kBK, blk * kRouteBlock, bar);
+        ptx::tma_load_2d(sa + kXBytes, &tmW, (kb0 + kb) * kBK, 0, bar);
         issued |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == g.stages) {
@@ -178,43 +206,99 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------------ epilogue, part 1:
+    // this CTA's partial logits (sum of its accumulators) into z_s (leader; finished with
+    // bias and temperature when the CTA is alone) or into the leader's receive buffer
     const int q = warp & 3;
     const int r = q * 32 + lane;  // token row of this block
+    for (int e = r; e < g.e_pad; e += kRouteBlock) bias_s[e] = (s.has_bias && e < s.E) ? w.bias[e] : 0.f;
     bool ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull), 0u, timeout_ns, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (lane == 0) ctl->vote[q] = ok ? 1 : 0;
     named_barrier(2, kRouteBlock);
     const bool all_ok = ctl->vote[0] && ctl->vote[1] && ctl->vote[2] && ctl->vote[3];
     float* z_s = reinterpret_cast<float*>(body);
-    uint32_t* mask_s = reinterpret_cast<uint32_t*>(z_s + kRouteBlock * (s.E + 1));
     const int ldz = s.E + 1;
+    const bool finish_here = g.split == 1;
+    const uint32_t recv_remote =
+        rank > 0 ? ptx::mapa(ptx::smem_u32(recv + ((int)rank - 1) * kRouteBlock * ldz + r * ldz), 0) : 0u;
     if (all_ok) {
       ptx::tc_fence_after();
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t z_row = ptx::smem_u32(z_s + r * ldz);
+      const uint32_t b_base = ptx::smem_u32(bias_s);
       const int used = kblocks < g.n_acc ? kblocks : g.n_acc;  // accumulators that were written
       for (int c = 0; c < g.e_pad; c += 16) {
-        float sum[16];
-        for (int a = 0; a < used; ++a) {
-          uint32_t v[16];
-          tmem_ld_16cols(t_row + (uint32_t)(a * g.e_pad + c), v);
-          ptx::tmem_ld_wait();
+        // every accumulator's 16 columns in flight at once, and the bias beside them
+        uint32_t v[kMaxAcc][16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sum[i] = a == 0 ? __uint_as_float(v[i]) : sum[i] + __uint_as_float(v[i]);
-        }
+        for (int a = 0; a < kMaxAcc; ++a)
+          if (a < used) tmem_ld_16cols(t_row + (uint32_t)(a * g.e_pad + c), v[a]);
+        float b[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) ld_shared_v4(b_base + 4u * (uint32_t)(c + i), b[i], b[i + 1], b[i + 2], b[i + 3]);
+        ptx::tmem_ld_wait();
+        float z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int e = c + i;
-          if (e < s.E) {
-            float z = sum[i];
-            if (s.has_bias) z += w.bias[e];
-            z_s[r * ldz + e] = z / s.tau;
-          }
+          z[i] = used > 0 ? __uint_as_float(v[0][i]) : 0.f;
+#pragma unroll
+          for (int a = 1; a < kMaxAcc; ++a)
+            if (a < used) z[i] += __uint_as_float(v[a][i]);
+          if (finish_here) z[i] = finish_logit(z[i], b[i], s.tau);
+        }
+        const int n = s.E - c < 16 ? s.E - c : 16;
+        if (rank == 0) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < n) st_shared_f32(z_row + 4u * (uint32_t)(c + i), z[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < n) ptx::st_cluster_u32(recv_remote + 4u * (uint32_t)(c + i), __float_as_uint(z[i]));
         }
       }
     } else {
       if (lane == 0 && q == 0) record_error(ws, MOE_ERR_TIMEOUT, 0x620u);
-      for (int e = 0; e < s.E; ++e) z_s[r * ldz + e] = 0.f;
+      for (int e = 0; e < s.E; ++e) {
+        if (rank == 0) z_s[r * ldz + e] = finish_here ? finish_logit(0.f, bias_s[e], s.tau) : 0.f;
+        else ptx::st_cluster_u32(recv_remote + 4u * (uint32_t)e, 0u);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (g.split > 1) ptx::cluster_sync();  // the partials of every CTA are in the leader's buffer
+  if (rank == 0 && warp >= 2) {
+    // ------------------------------------------------------------------ epilogue, part 2
+    // (leader): add the other CTAs' partials in rank order, bias, temperature; then the
+    // softmax / top-k / counting of route_finish
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    float* z_s = reinterpret_cast<float*>(body);
+    uint32_t* mask_s = reinterpret_cast<uint32_t*>(z_s + kRouteBlock * (s.E + 1));
+    const int ldz = s.E + 1;
+    if (g.split > 1) {
+      const uint32_t z_row = ptx::smem_u32(z_s + r * ldz);
+      const uint32_t r_row = ptx::smem_u32(recv + r * ldz);
+      const uint32_t b_base = ptx::smem_u32(bias_s);
+      for (int c = 0; c < s.E; c += 16) {
+        const int n = s.E - c < 16 ? s.E - c : 16;
+        float z[16], b[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) ld_shared_v4(b_base + 4u * (uint32_t)(c + i), b[i], b[i + 1], b[i + 2], b[i + 3]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = i < n ? ld_shared_f32(z_row + 4u * (uint32_t)(c + i)) : 0.f;
+        for (int rr = 1; rr < g.split; ++rr) {
+          const uint32_t part = r_row + (uint32_t)((rr - 1) * kRouteBlock * ldz * 4);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < n) z[i] += ld_shared_f32(part + 4u * (uint32_t)(c + i));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < n) st_shared_f32(z_row + 4u * (uint32_t)(c + i), finish_logit(z[i], b[i], s.tau));
+      }
     }
     route_finish(s, ws, blk, r, z_s, ldz, mask_s, /*bar_id=*/1);
   }
@@ -240,8 +324,9 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
 
 }  // namespace
 
-cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int64_t timeout_ns, cudaStream_t st) {
-  const RouteGeom g = route_geom(s);
+cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int num_sms, int64_t timeout_ns,
+                            cudaStream_t st) {
+  const RouteGeom g = route_geom(s, num_sms);
   CUtensorMap mx, mw;
   cudaError_t e;
   if ((e = make_tmap_bf16(&mx, w.x, (uint64_t)s.T, (uint64_t)s.d, kRouteBlock)) != cudaSuccess) return e;
@@ -249,8 +334,8 @@ cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int6
   if ((e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem)) !=
       cudaSuccess)
     return e;
-  route_tc_kernel<<<s.nblk, kThreads, g.smem, st>>>(mx, mw, s, ws, w, g, timeout_ns);
-  return cudaGetLastError();
+  return launch_kernel(route_tc_kernel, dim3((unsigned)(s.nblk * g.split)), dim3(kThreads), g.smem, st, false, g.split,
+                       mx, mw, s, ws, w, g, timeout_ns);
 }
 
 }  // namespace moe

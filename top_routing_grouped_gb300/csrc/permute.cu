@@ -6,13 +6,15 @@
 // §4 Dispatch: the all-to-all that sends each token to the device of its expert; with all
 // experts on one device it becomes this permutation inside HBM.
 //
-// One warp per token: the k destinations are computed by lanes 0..k-1 and broadcast, then
-// the row is read once with 16-byte vector loads and written k times (x is read once).
+// One warp per token: the row is read once with 16-byte vector loads (issued first), the k
+// destinations are computed by lanes 0..k-1 and broadcast, and the row is written k times
+// (x is read once).
 #include "device_common.cuh"
 
 namespace moe {
 
 constexpr int kPermWarps = 8;
+constexpr int kPermVec = 8;  // 16-byte vectors per lane in flight (a 4 KB row per warp)
 
 __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(Shape s, Ws ws, Weights w) {
   const int lane = threadIdx.x & 31;
@@ -25,6 +27,15 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(Shape s, Ws ws
   pdl_launch_dependents();
 
   for (int64_t t = warp; t < s.T; t += nwarps) {
+    // the row's first 32 x 8 vectors are requested before the routing lookups, so that the
+    // two latencies overlap
+    const int4* src = reinterpret_cast<const int4*>(reinterpret_cast<const char*>(w.x) + t * (int64_t)s.d * esz);
+    int4 buf[kPermVec];
+#pragma unroll
+    for (int u = 0; u < kPermVec; ++u) {
+      const int v = u * 32 + lane;
+      if (v < vecs) buf[u] = __ldcs(src + v);
+    }
     int64_t my_p = -1;
     if (lane < k) {
       const int64_t slot = t * k + lane;
@@ -46,24 +57,24 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(Shape s, Ws ws
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) dst[j] = __shfl_sync(0xffffffffu, my_p, j);
 
-    const int4* src = reinterpret_cast<const int4*>(reinterpret_cast<const char*>(w.x) + t * (int64_t)s.d * esz);
     int4* xp = reinterpret_cast<int4*>(ws.xp);
-    for (int v0 = 0; v0 < vecs; v0 += 32 * 4) {
-      int4 buf[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < vecs) buf[u] = __ldcs(src + v);
-      }
+    for (int v0 = 0;;) {
 #pragma unroll
       for (int j = 0; j < kMaxTopK; ++j) {
         if (j < k && dst[j] >= 0) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < kPermVec; ++u) {
             const int v = v0 + u * 32 + lane;
             if (v < vecs) xp[dst[j] * vecs + v] = buf[u];
           }
         }
+      }
+      v0 += 32 * kPermVec;
+      if (v0 >= vecs) break;
+#pragma unroll
+      for (int u = 0; u < kPermVec; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vecs) buf[u] = __ldcs(src + v);
       }
     }
   }

@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
 cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {
   const int64_t per = s.act_bf16 ? 8 : 4;
   int64_t blocks = (s.T * (s.d / per) + kCombThreads - 1) / kCombThreads;
-  const int64_t cap = (int64_t)num_sms * 8;
+  // enough blocks that every vector has its own thread on the movers' sizes (the grid-stride
+  // loop's iterations are not overlapped, so fewer, longer-lived threads are slower)
+  const int64_t cap = (int64_t)num_sms * 64;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const dim3 g((unsigned)blocks), b(kCombThreads);

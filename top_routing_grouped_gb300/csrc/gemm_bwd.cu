@@ -23,6 +23,7 @@
 
 #include "gemm_tc.h"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -48,7 +49,25 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl);
+// weight-gradient epilogue: each epilogue warp stages a 32 x 32 fp32 block (128-byte rows,
+// swizzled) and hands it to the TMA to store
+constexpr int kOutBlockBytes = 32 * 128;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kOutBlockBytes + sizeof(Ctl);
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 __host__ __device__ constexpr bool a_mn(int kind) { return kind == kBwdDW13 || kind == kBwdDW2; }
 __host__ __device__ constexpr bool k_grouped(int kind) { return kind == kBwdDW13 || kind == kBwdDW2; }
@@ -75,6 +94,32 @@ __device__ __forceinline__ void unpack8(uint4 raw, float* f) {
     const float2 v = __bfloat1622float2(h[i]);
     f[2 * i] = v.x;
     f[2 * i + 1] = v.y;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The dH epilogue's operands of one 16-column chunk of a row: h, and the two
+// pre-activations a = W1.x, b = W3.x (two 16-byte vectors each).
+struct DhChunk {
+  uint4 h[2], a[2], b[2];
+};
+
+__device__ __forceinline__ void dh_fetch(DhChunk& d, const __nv_bfloat16* hrow, const __nv_bfloat16* arow,
+                                         const __nv_bfloat16* brow, int c) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    d.h[i] = reinterpret_cast<const uint4*>(hrow + c)[i];
+    d.a[i] = reinterpret_cast<const uint4*>(arow + c)[i];
+    d.b[i] = reinterpret_cast<const uint4*>(brow + c)[i];
   }
 }
 
@@ -138,10 +183,12 @@ __device__ __forceinline__ BTile decode(const BwdArgs& a, int tile, int ngroups,
 template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB2, BwdArgs args, int64_t timeout_ns) {
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO1,
+                    const __grid_constant__ CUtensorMap tmO2, BwdArgs args, int64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(stages + kStages * kStageBytes);
+  uint8_t* out_blocks = stages + kStages * kStageBytes;  // 1024-byte aligned
+  Ctl* ctl = reinterpret_cast<Ctl*>(out_blocks + kEpiWarps * kOutBlockBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Shape& s = args.s;
@@ -302,55 +349,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+      const bool valid = r < bt.rows;
+      const int n0 = bt.n_idx * kTN;
+      // dH: the row's h / a / b are requested a chunk ahead of their use, the first chunk
+      // before the accumulator is ready, so that their latency hides behind the MMA
+      const int64_t p_dh = (int64_t)bt.row0 + r;
+      const __nv_bfloat16* hrow = reinterpret_cast<const __nv_bfloat16*>(ws.h) + p_dh * s.F + n0;
+      const __nv_bfloat16* arow = reinterpret_cast<const __nv_bfloat16*>(ws.a1) + p_dh * s.F + n0;
+      const __nv_bfloat16* brow = reinterpret_cast<const __nv_bfloat16*>(ws.a3) + p_dh * s.F + n0;
+      DhChunk pre[2];
+      if (kKind == kBwdDH && valid && n0 + c_beg < s.F) dh_fetch(pre[0], hrow, arow, brow, c_beg);
       ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull[acc]), acc_phase, timeout_ns, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTN);
-      const bool valid = r < bt.rows;
-      const int n0 = bt.n_idx * kTN;
       if (kKind == kBwdDH) {
-        const int64_t p = (int64_t)bt.row0 + r;
+        const int64_t p = p_dh;
         const int F = s.F;
         const float g = valid ? ws.gate_perm[p] : 0.f;
-        const __nv_bfloat16* hrow = reinterpret_cast<const __nv_bfloat16*>(ws.h) + p * F + n0;
-        const __nv_bfloat16* arow = reinterpret_cast<const __nv_bfloat16*>(ws.a1) + p * F + n0;
-        const __nv_bfloat16* brow = reinterpret_cast<const __nv_bfloat16*>(ws.a3) + p * F + n0;
         __nv_bfloat16* darow = reinterpret_cast<__nv_bfloat16*>(ws.dab) + p * 2 * F + n0;
         float dg = 0.f;
-#pragma unroll 1
-        for (int c = c_beg; c < c_end; c += 32) {
-          if (n0 + c >= F) break;  // uniform across the warp
-          uint32_t v[32];
-          ptx::tmem_ld_32cols(t_row + c, v);
-          ptx::tmem_ld_wait();
-          if (valid) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float hv[8], av[8], bv[8];
-              unpack8(*reinterpret_cast<const uint4*>(hrow + c + 8 * u), hv);
-              unpack8(*reinterpret_cast<const uint4*>(arow + c + 8 * u), av);
-              unpack8(*reinterpret_cast<const uint4*>(brow + c + 8 * u), bv);
-              uint4 oa, ob;
-              uint32_t* wa = reinterpret_cast<uint32_t*>(&oa);
-              uint32_t* wb = reinterpret_cast<uint32_t*>(&ob);
+        for (int i = 0; i < (kTN / 2) / 16; ++i) {
+          const int c = c_beg + 16 * i;
+          if (i + 1 < (kTN / 2) / 16 && valid && n0 + c + 16 < F) dh_fetch(pre[(i + 1) & 1], hrow, arow, brow, c + 16);
+          if (n0 + c < F) {  // uniform across the warp
+            uint32_t v[16];
+            tmem_ld_16cols(t_row + c, v);
+            ptx::tmem_ld_wait();
+            if (valid) {
+              const DhChunk& d = pre[i & 1];
 #pragma unroll
-              for (int i = 0; i < 8; i += 2) {
-                float da[2], db[2];
+              for (int u = 0; u < 2; ++u) {
+                float hv[8], av[8], bv[8];
+                unpack8(d.h[u], hv);
+                unpack8(d.a[u], av);
+                unpack8(d.b[u], bv);
+                uint4 oa, ob;
+                uint32_t* wa = reinterpret_cast<uint32_t*>(&oa);
+                uint32_t* wb = reinterpret_cast<uint32_t*>(&ob);
 #pragma unroll
-                for (int z = 0; z < 2; ++z) {
-                  const float dh = __uint_as_float(v[8 * u + i + z]);
-                  dg += hv[i + z] * dh;
-                  const float a = av[i + z];
-                  const float sg = sigmoid_fast(a);
-                  da[z] = g * dh * bv[i + z] * sg * (1.0f + a * (1.0f - sg));
-                  db[z] = g * dh * a * sg;
+                for (int e2 = 0; e2 < 8; e2 += 2) {
+                  float da[2], db[2];
+#pragma unroll
+                  for (int z = 0; z < 2; ++z) {
+                    const float dh = __uint_as_float(v[8 * u + e2 + z]);
+                    dg += hv[e2 + z] * dh;
+                    const float a = av[e2 + z];
+                    const float sg = sigmoid_fast(a);
+                    da[z] = g * dh * bv[e2 + z] * sg * (1.0f + a * (1.0f - sg));
+                    db[z] = g * dh * a * sg;
+                  }
+                  wa[e2 / 2] = pack2(da[0], da[1]);
+                  wb[e2 / 2] = pack2(db[0], db[1]);
                 }
-                wa[i / 2] = pack2(da[0], da[1]);
-                wb[i / 2] = pack2(db[0], db[1]);
+                *reinterpret_cast<uint4*>(darow + c + 8 * u) = oa;
+                *reinterpret_cast<uint4*>(darow + F + c + 8 * u) = ob;
               }
-              *reinterpret_cast<uint4*>(darow + c + 8 * u) = oa;
-              *reinterpret_cast<uint4*>(darow + F + c + 8 * u) = ob;
             }
           }
         }
@@ -379,13 +435,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // weight gradients, fp32 row-major; an expert without rows gets zeros
-        const int m = bt.row0 + r;
-        float* out;
-        if (kKind == kBwdDW13)
-          out = (m < s.F ? args.dw_a + ((int64_t)bt.e * s.F + m) * s.d : args.dw_b + ((int64_t)bt.e * s.F + (m - s.F)) * s.d) + n0;
-        else
-          out = args.dw_a + ((int64_t)bt.e * s.d + m) * s.F + n0;
+        // weight gradients, fp32 row-major; an expert without rows gets zeros.  This warp's
+        // 32 rows x 32 columns at a time go through its staging block to a TMA store (full
+        // 128-byte lines, asynchronous), row `lane` written by lane `lane`, its 16-byte
+        // chunk j at j ^ (lane % 8) (the 128-byte swizzle)
+        const int mblk = bt.row0 + q * 32;  // first output row of this warp's block
+        const bool blk_valid = mblk < M;    // M is a multiple of 64: whole blocks only
+        const CUtensorMap* om = &tmO1;
+        int orow;
+        if (kKind == kBwdDW13) {
+          if (mblk >= s.F) om = &tmO2;
+          orow = bt.e * s.F + (mblk >= s.F ? mblk - s.F : mblk);
+        } else {
+          orow = bt.e * s.d + mblk;
+        }
+        const uint32_t ob = ptx::smem_u32(out_blocks + (warp - kEpiWarp0) * kOutBlockBytes);
 #pragma unroll 1
         for (int c = c_beg; c < c_end; c += 32) {
           if (n0 + c >= N) break;
@@ -397,12 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          if (valid) {
-            float4* o4 = reinterpret_cast<float4*>(out + c);
+          if (blk_valid) {
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the block
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                                  __uint_as_float(v[4 * i + 3]));
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(ob + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16), v[4 * j], v[4 * j + 1],
+                           v[4 * j + 2], v[4 * j + 3]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(om, n0 + c, orow, ob);
+              bulk_commit();
+            }
           }
         }
       }
@@ -415,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
       record_error(ws, MOE_ERR_TIMEOUT, 0x820u + kKind);
     }
+    if (k_grouped(kKind) && lane == 0) bulk_wait_all();  // this warp's stores are complete
   }
 
   __syncthreads();
@@ -437,12 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int kKind>
-cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const BwdArgs& args,
-                        int num_sms, int64_t timeout_ns, bool pdl, cudaStream_t st) {
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o1,
+                        const CUtensorMap& o2, const BwdArgs& args, int num_sms, int64_t timeout_ns, bool pdl,
+                        cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(gemm_bwd_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_kernel(gemm_bwd_kernel<kKind>, dim3(num_sms), dim3(kThreads), kSmemBytes, st, pdl, 1, a, b, b2, args,
-                       timeout_ns);
+  return launch_kernel(gemm_bwd_kernel<kKind>, dim3(num_sms), dim3(kThreads), kSmemBytes, st, pdl, 1, a, b, b2, o1, o2,
+                       args, timeout_ns);
 }
 
 }  // namespace
@@ -450,27 +523,30 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 cudaError_t launch_gemm_bwd(int kind, const Shape& s, const Ws& ws, const Weights& w, float* dw_a, float* dw_b,
                             int num_sms, int64_t timeout_ns, bool pdl, cudaStream_t st) {
   BwdArgs args{s, ws, dw_a, dw_b};
-  CUtensorMap ma, mb, mb2;
+  CUtensorMap ma, mb, mb2, mo1, mo2;
   cudaError_t e;
   const uint64_t N = (uint64_t)s.N, d = (uint64_t)s.d, F = (uint64_t)s.F, E = (uint64_t)s.E;
   switch (kind) {
     case kBwdDH:
       if ((e = make_tmap_bf16(&ma, ws.dyp, N, d, 128)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb, w.w2, E * d, F, 64)) != cudaSuccess) return e;
-      return launch_kind<kBwdDH>(ma, mb, mb, args, num_sms, timeout_ns, pdl, st);
+      return launch_kind<kBwdDH>(ma, mb, mb, mb, mb, args, num_sms, timeout_ns, pdl, st);
     case kBwdDX:
       if ((e = make_tmap_bf16(&ma, ws.dab, N, 2 * F, 128)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb, w.w1, E * F, d, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb2, w.w3, E * F, d, 64)) != cudaSuccess) return e;
-      return launch_kind<kBwdDX>(ma, mb, mb2, args, num_sms, timeout_ns, pdl, st);
+      return launch_kind<kBwdDX>(ma, mb, mb2, mb, mb, args, num_sms, timeout_ns, pdl, st);
     case kBwdDW13:
       if ((e = make_tmap_bf16(&ma, ws.dab, N, 2 * F, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb, ws.xp, N, d, 64)) != cudaSuccess) return e;
-      return launch_kind<kBwdDW13>(ma, mb, mb, args, num_sms, timeout_ns, pdl, st);
+      if ((e = make_tmap_f32_rows128(&mo1, dw_a, E * F, d, 32)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32_rows128(&mo2, dw_b, E * F, d, 32)) != cudaSuccess) return e;
+      return launch_kind<kBwdDW13>(ma, mb, mb, mo1, mo2, args, num_sms, timeout_ns, pdl, st);
     case kBwdDW2:
       if ((e = make_tmap_bf16(&ma, ws.dop, N, d, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb, ws.h, N, F, 64)) != cudaSuccess) return e;
-      return launch_kind<kBwdDW2>(ma, mb, mb, args, num_sms, timeout_ns, pdl, st);
+      if ((e = make_tmap_f32_rows128(&mo1, dw_a, E * d, F, 32)) != cudaSuccess) return e;
+      return launch_kind<kBwdDW2>(ma, mb, mb, mo1, mo1, args, num_sms, timeout_ns, pdl, st);
   }
   return cudaErrorInvalidValue;
 }

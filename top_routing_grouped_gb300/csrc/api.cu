@@ -10,6 +10,7 @@
 #include <string>
 
 #include "moe_internal.h"
+#include "gemm_bwd.h"
 #include "gemm_tc.h"
 
 struct moe_plan_s {
@@ -392,8 +393,13 @@ moe_status moe_backward_stage(moe_plan_t plan, int32_t stage, const void* x, con
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0: e = moe::launch_gather_dy(s, ws, dy, plan->num_sms, false, cs); break;
-    case 1: e = moe::launch_gemm_bwd(moe::kBwdDH, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
-    case 2: e = moe::launch_gemm_bwd(moe::kBwdDX, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
+    case 1:
+    case 2: {
+      const int kind = stage == 1 ? moe::kBwdDH : moe::kBwdDX;
+      e = plan->pair ? moe::launch_gemm_bwd_pair(kind, s, ws, w, plan->num_sms, plan->timeout_ns, pdl, cs)
+                     : moe::launch_gemm_bwd(kind, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs);
+      break;
+    }
     case 3: e = moe::launch_gemm_bwd(moe::kBwdDW13, s, ws, w, dw1, dw3, plan->num_sms, plan->timeout_ns, pdl, cs); break;
     case 4: e = moe::launch_gemm_bwd(moe::kBwdDW2, s, ws, w, dw2, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
     case 5: e = moe::launch_router_bwd(s, ws, aux_weight, 2 * ((s.F + 255) / 256), pdl, cs); break;

@@ -115,8 +115,10 @@ WsLayout ws_layout(const Shape& s) {
     L.dgp = take(N * nt * 4);
     L.dxslot = take(N * (size_t)s.d * 2);
     L.dlogit = take((size_t)s.T * E * 4);
+    L.dl_hi = take((size_t)s.T * moe::dlogit_cols(s) * 2);
+    L.dl_lo = take((size_t)s.T * moe::dlogit_cols(s) * 2);
     L.dwr_part = take(chunks * E * (size_t)s.d * 4);
-    L.dwr_part_b = take(chunks * E * 4);
+    L.dwr_part_b = take(nb * E * 4);
   }
   L.total = off;
   return L;
@@ -158,6 +160,8 @@ Ws ws_bind(const Shape& s, void* base) {
     w.dgp = reinterpret_cast<float*>(b + L.dgp);
     w.dxslot = b + L.dxslot;
     w.dlogit = reinterpret_cast<float*>(b + L.dlogit);
+    w.dl_hi = b + L.dl_hi;
+    w.dl_lo = b + L.dl_lo;
     w.dwr_part = reinterpret_cast<float*>(b + L.dwr_part);
     w.dwr_part_b = reinterpret_cast<float*>(b + L.dwr_part_b);
   }
@@ -403,10 +407,11 @@ moe_status moe_backward_stage(moe_plan_t plan, int32_t stage, const void* x, con
     case 3: e = moe::launch_gemm_bwd(moe::kBwdDW13, s, ws, w, dw1, dw3, plan->num_sms, plan->timeout_ns, pdl, cs); break;
     case 4: e = moe::launch_gemm_bwd(moe::kBwdDW2, s, ws, w, dw2, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
     case 5: e = moe::launch_router_bwd(s, ws, aux_weight, 2 * ((s.F + 255) / 256), pdl, cs); break;
-    case 6: e = moe::launch_dx(s, ws, w_router, dx, pdl, cs); break;
+    case 6: e = moe::launch_dx_tc(s, ws, w_router, dx, plan->timeout_ns, pdl, cs); break;
     case 7:
-      e = moe::launch_dwr(s, ws, x, ws.dwr_part, ws.dwr_part_b, dw_router, plan->shape.has_bias ? dbias : nullptr,
-                          plan->num_sms, pdl, cs);
+      e = moe::launch_dwr_tc(s, ws, x, plan->timeout_ns, pdl, cs);
+      if (e == cudaSuccess)
+        e = moe::launch_dwr_reduce(s, ws, dw_router, plan->shape.has_bias ? dbias : nullptr, plan->num_sms, true, cs);
       break;
   }
   if (e != cudaSuccess) {

@@ -7,9 +7,11 @@
 //   router_bwd   dg_j = sum of the per-tile partials of dy . o  (fixed order);
 //                dp_e = sum_j [idx_j = e] dg_j (renormalised gates: (dg_j - sum g dg) / S)
 //                       + alpha E f_e / T;  dz = p (dp - p . dp);  dlogit = dz / tau
-//   dx           dx[t] = sum_j dXslot[t k + j] + sum_e dlogit[t, e] W_r[e]
-//   dwr          dW_r[e] = sum_t dlogit[t, e] x[t],  dbias[e] = sum_t dlogit[t, e]
-//                (split over token chunks; the chunks are added in a fixed order)
+//   dx           dx[t] = sum_j dXslot[t k + j] + sum_e dlogit[t, e] W_r[e] (tensor cores,
+//                bwd_tc.cu)
+//   dwr          dW_r[e] = sum_t dlogit[t, e] x[t] (tensor cores, bwd_tc.cu, over token
+//                chunks) and dbias[e] = sum_t dlogit[t, e] (per router block, here); the
+//                partials are added in a fixed order
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -114,131 +116,47 @@ __global__ void __launch_bounds__(128) router_bwd_kernel(Shape s, Ws ws, float a
   }
   float pdp = 0.f;
   for (int e = 0; e < E; ++e) pdp += pt[e] * dp[e];
-  for (int e = 0; e < E; ++e) ws.dlogit[t * E + e] = pt[e] * (dp[e] - pdp) / s.tau;
-}
-
-// dx[t, c] = sum_j dXslot[t k + j, c] + sum_e dlogit[t, e] W_r[e, c].  Tiles of 64 tokens x
-// 128 columns, 256 threads each holding 4 tokens x 8 columns in registers; dlogit and W_r
-// staged in shared memory over E in chunks of 32.
-constexpr int kDxT = 64, kDxC = 128, kDxE = 32;
-__global__ void __launch_bounds__(256) dx_kernel(Shape s, Ws ws, const void* w_router, float* dx) {
-  __shared__ float zl[kDxE][kDxT + 4];  // transposed: zl[e][t]
-  __shared__ float wr[kDxE][kDxC + 4];
-  const int tid = threadIdx.x;
-  const int tg = tid / 16, cg = tid % 16;  // tokens tg*4.., columns cg*8..
-  const int64_t t0 = (int64_t)blockIdx.y * kDxT;
-  const int c0 = blockIdx.x * kDxC;
-  pdl_wait();
-  pdl_launch_dependents();
-  float acc[4][8];
+  // dlogit in fp32, and as two bf16 terms for the tensor-core router-weight gradient
+  const int ec = dlogit_cols(s);  // a multiple of 64: whole 16-byte vectors of 8
+  uint4* hi = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.dl_hi) + t * ec);
+  uint4* lo = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.dl_lo) + t * ec);
+  for (int e0 = 0; e0 < ec; e0 += 8) {
+    uint4 vh, vl;
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&vh);
+    __nv_bfloat162* l2 = reinterpret_cast<__nv_bfloat162*>(&vl);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+    for (int u = 0; u < 4; ++u) {
+      float v[2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int e0 = 0; e0 < s.E; e0 += kDxE) {
-    for (int i = tid; i < kDxT * kDxE; i += 256) {
-      const int tt = i / kDxE, ee = i % kDxE;
-      const int64_t t = t0 + tt;
-      zl[ee][tt] = (t < s.T && e0 + ee < s.E) ? ws.dlogit[t * s.E + e0 + ee] : 0.f;
-    }
-    for (int i = tid; i < kDxE * kDxC; i += 256) {
-      const int ee = i / kDxC, cc = i % kDxC;
-      wr[ee][cc] = (e0 + ee < s.E && c0 + cc < s.d) ? load_act(w_router, 1, (int64_t)(e0 + ee) * s.d + c0 + cc) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int ee = 0; ee < kDxE; ++ee) {
-      const float4 za = *reinterpret_cast<const float4*>(&zl[ee][tg * 4]);
-      const float4 w0 = *reinterpret_cast<const float4*>(&wr[ee][cg * 8]);
-      const float4 w1 = *reinterpret_cast<const float4*>(&wr[ee][cg * 8 + 4]);
-      const float zv[4] = {za.x, za.y, za.z, za.w};
-      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(zv[i], wv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t t = t0 + tg * 4 + i;
-    if (t >= s.T) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + cg * 8 + j;
-      if (c >= s.d) continue;
-      float v = acc[i][j];
-      for (int q = 0; q < s.k; ++q)
-        v += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(ws.dxslot)[(t * s.k + q) * s.d + c]);
-      dx[t * s.d + c] = v;
-    }
-  }
-}
-
-// Partial router-weight gradients over chunks of kDwrTok tokens: part[chunk][e][c] and
-// part_b[chunk][e] for a tile of 64 experts x 128 columns (each thread 4 experts x 8
-// columns); a second kernel adds the chunks in order.
-constexpr int kDwrTok = 512, kDwrE = 64, kDwrC = 128, kDwrK = 32;
-__global__ void __launch_bounds__(256) dwr_partial_kernel(Shape s, Ws ws, const void* x, float* part, float* part_b) {
-  __shared__ float zl[kDwrK][kDwrE + 4];
-  __shared__ float xs[kDwrK][kDwrC + 4];
-  const int tid = threadIdx.x;
-  const int eg = tid / 16, cg = tid % 16;
-  const int c0 = blockIdx.x * kDwrC;
-  const int e0 = blockIdx.y * kDwrE;
-  const int chunk = blockIdx.z;
-  const int64_t tbeg = (int64_t)chunk * kDwrTok;
-  pdl_wait();
-  pdl_launch_dependents();
-  float acc[4][8], bacc[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    bacc[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  }
-  for (int64_t tb = tbeg; tb < tbeg + kDwrTok && tb < s.T; tb += kDwrK) {
-    for (int i = tid; i < kDwrK * kDwrE; i += 256) {
-      const int tt = i / kDwrE, ee = i % kDwrE;
-      const int64_t t = tb + tt;
-      zl[tt][ee] = (t < s.T && e0 + ee < s.E) ? ws.dlogit[t * s.E + e0 + ee] : 0.f;
-    }
-    for (int i = tid; i < kDwrK * kDwrC; i += 256) {
-      const int tt = i / kDwrC, cc = i % kDwrC;
-      const int64_t t = tb + tt;
-      xs[tt][cc] = (t < s.T && c0 + cc < s.d) ? load_act(x, s.act_bf16, t * s.d + c0 + cc) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int tt = 0; tt < kDwrK; ++tt) {
-      const float4 za = *reinterpret_cast<const float4*>(&zl[tt][eg * 4]);
-      const float4 x0 = *reinterpret_cast<const float4*>(&xs[tt][cg * 8]);
-      const float4 x1 = *reinterpret_cast<const float4*>(&xs[tt][cg * 8 + 4]);
-      const float zv[4] = {za.x, za.y, za.z, za.w};
-      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bacc[i] += zv[i];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(zv[i], xv[j], acc[i][j]);
+      for (int z = 0; z < 2; ++z) {
+        const int e = e0 + 2 * u + z;
+        v[z] = e < E ? pt[e] * (dp[e] - pdp) / s.tau : 0.f;
+        if (e < E) ws.dlogit[t * E + e] = v[z];
       }
+      h2[u] = __floats2bfloat162_rn(v[0], v[1]);
+      const float2 hf = __bfloat1622float2(h2[u]);
+      l2[u] = __floats2bfloat162_rn(v[0] - hf.x, v[1] - hf.y);
     }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = e0 + eg * 4 + i;
-    if (e >= s.E) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + cg * 8 + j;
-      if (c < s.d) part[((int64_t)chunk * s.E + e) * s.d + c] = acc[i][j];
-    }
-    if (blockIdx.x == 0 && cg == 0) part_b[(int64_t)chunk * s.E + e] = bacc[i];
+    hi[e0 / 8] = vh;
+    lo[e0 / 8] = vl;
   }
 }
 
+// The router-bias gradient of each router block: part_b[blk, e] = sum over the block's
+// tokens of dlogit[t, e], in token order.
+__global__ void __launch_bounds__(128) dbias_block_kernel(Shape s, Ws ws) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t t0 = (int64_t)blockIdx.x * 128;
+  for (int e = threadIdx.x; e < s.E; e += 128) {
+    float v = 0.f;
+    for (int r = 0; r < 128 && t0 + r < s.T; ++r) v += ws.dlogit[(t0 + r) * s.E + e];
+    ws.dwr_part_b[(int64_t)blockIdx.x * s.E + e] = v;
+  }
+}
+
+// dW_r = sum of the token-chunk partials in chunk order; dbias = sum of the router-block
+// partials in block order
 __global__ void __launch_bounds__(256) dwr_reduce_kernel(Shape s, const float* part, const float* part_b, int chunks,
                                                          float* dwr, float* dbias) {
   pdl_wait();
@@ -252,12 +170,10 @@ __global__ void __launch_bounds__(256) dwr_reduce_kernel(Shape s, const float* p
   if (dbias && blockIdx.x == 0)
     for (int e = threadIdx.x; e < s.E; e += 256) {
       float v = 0.f;
-      for (int ch = 0; ch < chunks; ++ch) v += part_b[(int64_t)ch * s.E + e];
+      for (int b = 0; b < s.nblk; ++b) v += part_b[(int64_t)b * s.E + e];
       dbias[e] = v;
     }
 }
-
-int dwr_chunks(const Shape& s) { return (int)((s.T + kDwrTok - 1) / kDwrTok); }
 
 cudaError_t launch_gather_dy(const Shape& s, const Ws& ws, const void* dy, int num_sms, bool pdl, cudaStream_t st) {
   int64_t blocks = (s.T + kGatherWarps - 1) / kGatherWarps;
@@ -272,19 +188,13 @@ cudaError_t launch_router_bwd(const Shape& s, const Ws& ws, float alpha, int n_t
   return launch_kernel(router_bwd_kernel, dim3((unsigned)s.nblk), dim3(128), smem, st, pdl, 1, s, ws, alpha, n_tiles_dh);
 }
 
-cudaError_t launch_dx(const Shape& s, const Ws& ws, const void* w_router, float* dx, bool pdl, cudaStream_t st) {
-  const dim3 g((unsigned)((s.d + kDxC - 1) / kDxC), (unsigned)((s.T + kDxT - 1) / kDxT));
-  return launch_kernel(dx_kernel, g, dim3(256), 0, st, pdl, 1, s, ws, w_router, dx);
-}
-
-cudaError_t launch_dwr(const Shape& s, const Ws& ws, const void* x, float* part, float* part_b, float* dwr, float* dbias,
-                       int num_sms, bool pdl, cudaStream_t st) {
-  const int chunks = dwr_chunks(s);
-  const dim3 g((unsigned)((s.d + kDwrC - 1) / kDwrC), (unsigned)((s.E + kDwrE - 1) / kDwrE), (unsigned)chunks);
-  cudaError_t e = launch_kernel(dwr_partial_kernel, g, dim3(256), 0, st, pdl, 1, s, ws, x, part, part_b);
+cudaError_t launch_dwr_reduce(const Shape& s, const Ws& ws, float* dwr, float* dbias, int num_sms, bool pdl,
+                              cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (dbias) e = launch_kernel(dbias_block_kernel, dim3((unsigned)s.nblk), dim3(128), 0, st, pdl, 1, s, ws);
   if (e != cudaSuccess) return e;
-  return launch_kernel(dwr_reduce_kernel, dim3((unsigned)num_sms * 2), dim3(256), 0, st, true, 1, s,
-                       (const float*)part, (const float*)part_b, chunks, dwr, dbias);
+  return launch_kernel(dwr_reduce_kernel, dim3((unsigned)num_sms * 2), dim3(256), 0, st, pdl, 1, s,
+                       (const float*)ws.dwr_part, (const float*)ws.dwr_part_b, dwr_chunks(s), dwr, dbias);
 }
 
 }  // namespace moe

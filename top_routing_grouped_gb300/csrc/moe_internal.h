@@ -66,16 +66,22 @@ struct Ws {
   float* dgp;           // [N, 2 ceil(F/256)] partial dy . o per 128-column half tile
   void* dxslot;         // [N, d] bf16: expert-input gradient of each routed slot (token order)
   float* dlogit;        // [T, E]
-  float* dwr_part;      // [ceil(T/256), E, d] router-weight gradient partials
-  float* dwr_part_b;    // [ceil(T/256), E]
+  void* dl_hi;          // [T, dlogit_cols] bf16: dlogit rounded (zero columns past E)
+  void* dl_lo;          // [T, dlogit_cols] bf16: dlogit - dl_hi, rounded
+  float* dwr_part;      // [dwr_chunks, E, d] router-weight gradient partials (token chunks)
+  float* dwr_part_b;    // [nblk, E] router-bias gradient partials (router blocks)
 };
 
 // Fixed layout of one workspace: byte offsets of each region.
 struct WsLayout {
   size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
       grp_expert, grp_mtile0, grp_mpre, grp_ppre, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
-      yslot, a1, a3, probs, dyp, dop, dab, dgp, dxslot, dlogit, dwr_part, dwr_part_b, total;
+      yslot, a1, a3, probs, dyp, dop, dab, dgp, dxslot, dlogit, dl_hi, dl_lo, dwr_part, dwr_part_b, total;
 };
+
+// Columns of the bf16 dlogit terms: E rounded up to 64 (a whole 128-byte TMA box).
+__host__ __device__ inline int dlogit_cols(const Shape& s) { return (s.E + 63) / 64 * 64; }
+constexpr int kDwrMaxChunks = 32;  // token chunks of the router-weight gradient
 
 WsLayout ws_layout(const Shape& s);
 Ws ws_bind(const Shape& s, void* base);
@@ -130,10 +136,12 @@ cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int n
 
 cudaError_t launch_gather_dy(const Shape& s, const Ws& ws, const void* dy, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_router_bwd(const Shape& s, const Ws& ws, float alpha, int n_tiles_dh, bool pdl, cudaStream_t st);
-cudaError_t launch_dx(const Shape& s, const Ws& ws, const void* w_router, float* dx, bool pdl, cudaStream_t st);
-cudaError_t launch_dwr(const Shape& s, const Ws& ws, const void* x, float* part, float* part_b, float* dwr, float* dbias,
-                       int num_sms, bool pdl, cudaStream_t st);
+// the chunk partials of the router-weight gradient (and the block partials of the bias
+// gradient) added in order
+cudaError_t launch_dwr_reduce(const Shape& s, const Ws& ws, float* dwr, float* dbias, int num_sms, bool pdl,
+                              cudaStream_t st);
 int dwr_chunks(const Shape& s);
+int dwr_chunk_tokens(const Shape& s);
 
 // Plan internals for entry points defined outside api.cu.
 const Shape* plan_shape(moe_plan_t plan);

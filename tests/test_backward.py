@@ -51,21 +51,24 @@ def run_backward(moe, s, inp, alpha, path="auto"):
     return plan, ws, dy, {k: v.cpu().numpy() for k, v in out.items()}
 
 
-@pytest.mark.parametrize("dims, alpha, renorm, bias", [
-    ((300, 256, 8, 2, 192), 0.0, False, True),     # ragged T, 3 column tiles of H, bias
-    ((256, 128, 16, 4, 128), 0.5, False, False),   # balancing-loss gradient on
-    ((200, 192, 8, 3, 256), 0.25, True, True),     # renormalised gates
-    ((130, 128, 32, 2, 64), 0.0, False, False),    # experts with 0..few rows (zero dW)
-    ((1024, 1024, 8, 2, 1024), 0.1, False, True),  # medium: many K blocks per expert, 4 H tiles
+@pytest.mark.parametrize("dims, alpha, renorm, bias, path", [
+    ((300, 256, 8, 2, 192), 0.0, False, True, "auto"),     # ragged T, 3 column tiles of H, bias
+    ((256, 128, 16, 4, 128), 0.5, False, False, "auto"),   # balancing-loss gradient on
+    ((200, 192, 8, 3, 256), 0.25, True, True, "auto"),     # renormalised gates
+    ((130, 128, 32, 2, 64), 0.0, False, False, "auto"),    # experts with 0..few rows (zero dW)
+    ((1024, 1024, 8, 2, 1024), 0.1, False, True, "auto"),  # medium: many K blocks per expert, 4 H tiles
+    # the one-CTA backward GEMMs (MOE_PATH_TC_1SM)
+    ((300, 256, 8, 2, 192), 0.0, False, True, "tc1"),
+    ((130, 128, 32, 2, 64), 0.0, False, False, "tc1"),
 ])
-def test_backward_matches_oracle(dims, alpha, renorm, bias):
+def test_backward_matches_oracle(dims, alpha, renorm, bias, path):
     from top_routing_grouped_gb300 import moe
     import parity
     T, d, E, k, F = dims
     s = MoEShape("bwd", T=T, d=d, E=E, k=k, F=F, dtype="bf16", tau=0.8, renorm=renorm)
     inp = make_inputs(s, seed=21)
     inp.bias = torch.linspace(-0.4, 0.4, E, dtype=torch.float32) if bias else None
-    plan, ws, dy, got = run_backward(moe, s, inp, alpha)
+    plan, ws, dy, got = run_backward(moe, s, inp, alpha, path=path)
     host = inp.numpy_for_oracle()
     orc = oracle.Oracle(T, d, E, k, F, tau=s.tau, dtype="bf16", renorm=renorm)
     z, _, oidx, _ = orc.router(host["x"], host["wr"], host["bias"])
@@ -76,7 +79,7 @@ def test_backward_matches_oracle(dims, alpha, renorm, bias):
     names = ["dx", "dwr", "dw1", "dw3", "dw2"] + (["dbias"] if bias else [])
     errs = {n: rel_err(got[n], ref[n]) for n in names}
     nerrs = {n: norm_err(got[n], ref[n]) for n in names}
-    print(f"\n[backward {dims} alpha={alpha} renorm={renorm}] "
+    print(f"\n[backward {dims} alpha={alpha} renorm={renorm} path={path}] "
           + " ".join(f"{n}={errs[n]:.2e}/{nerrs[n]:.2e}" for n in names))
     for n in names:
         assert errs[n] <= TOL, f"{n}: {errs[n]}"

@@ -404,8 +404,15 @@ moe_status moe_backward_stage(moe_plan_t plan, int32_t stage, const void* x, con
                      : moe::launch_gemm_bwd(kind, s, ws, w, nullptr, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs);
       break;
     }
-    case 3: e = moe::launch_gemm_bwd(moe::kBwdDW13, s, ws, w, dw1, dw3, plan->num_sms, plan->timeout_ns, pdl, cs); break;
-    case 4: e = moe::launch_gemm_bwd(moe::kBwdDW2, s, ws, w, dw2, nullptr, plan->num_sms, plan->timeout_ns, pdl, cs); break;
+    case 3:
+    case 4: {
+      const int kind = stage == 3 ? moe::kBwdDW13 : moe::kBwdDW2;
+      float* a = stage == 3 ? dw1 : dw2;
+      float* b = stage == 3 ? dw3 : nullptr;
+      e = plan->pair ? moe::launch_gemm_dw_pair(kind, s, ws, a, b, plan->num_sms, plan->timeout_ns, pdl, cs)
+                     : moe::launch_gemm_bwd(kind, s, ws, w, a, b, plan->num_sms, plan->timeout_ns, pdl, cs);
+      break;
+    }
     case 5: e = moe::launch_router_bwd(s, ws, aux_weight, 2 * ((s.F + 255) / 256), pdl, cs); break;
     case 6: e = moe::launch_dx_tc(s, ws, w_router, dx, plan->timeout_ns, pdl, cs); break;
     case 7:

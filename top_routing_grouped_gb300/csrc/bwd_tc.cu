@@ -19,6 +19,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "bwd_common.cuh"
 #include "gemm_bwd.h"
 #include "gemm_tc.h"
 #include "tc_ptx.cuh"
@@ -26,11 +27,12 @@
 namespace moe {
 namespace {
 
+using namespace bwd;
+
 constexpr int kBK = 64;        // tokens per K block
 constexpr int kTM = 128;       // experts per tile
 constexpr int kTN = 128;       // columns per tile
 constexpr int kStages = 2;
-constexpr int kBoxBytes = 64 * kBK * 2;              // one 64 x 64 MN-major box
 constexpr int kABytes = 2 * kBoxBytes;               // 128 experts, one term
 constexpr int kBBytes = 2 * kBoxBytes;               // 128 columns
 constexpr int kStageBytes = 2 * kABytes + kBBytes;   // hi, lo, x: 48 KB
@@ -46,15 +48,6 @@ struct Ctl {
 };
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl);
 
-__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(kBoxBytes >> 4) << 16;  // leading: next 64-wide MN block
-  d |= (uint64_t)(1024 >> 4) << 32;       // stride: next 8 K rows
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
 
 __global__ void __launch_bounds__(kThreads) dwr_tc_kernel(const __grid_constant__ CUtensorMap tmHi,
                                                          const __grid_constant__ CUtensorMap tmLo,
@@ -228,13 +221,7 @@ constexpr int kDxThreads = 320;
 constexpr int kDxEpiWarps = 8;
 constexpr size_t kDxSmemBytes = 1024 + (size_t)kDxStageBytes + kDxEpiWarps * (size_t)kDxXposeBytes + sizeof(Ctl);
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float& a, float& b, float& c, float& d) {
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr) : "memory");
-}
 
 __global__ void __launch_bounds__(kDxThreads) dx_tc_kernel(const __grid_constant__ CUtensorMap tmHi,
                                                         const __grid_constant__ CUtensorMap tmLo,
@@ -351,18 +338,15 @@ __global__ void __launch_bounds__(kDxThreads) dx_tc_kernel(const __grid_constant
         uint32_t v[32];
         ptx::tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
         ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_shared_v4(xb + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16), v[4 * j], v[4 * j + 1],
-                       v[4 * j + 2], v[4 * j + 3]);
+        stage_row32(xb, lane, v);
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int br = 8 * i + (lane >> 2);  // row of the block
           const int64_t t = t0 + q * 32 + br;
           float a[8];
-          ld_shared_v4(xb + (uint32_t)br * 128u + (uint32_t)(((cg >> 2) ^ (br & 7)) * 16), a[0], a[1], a[2], a[3]);
-          ld_shared_v4(xb + (uint32_t)br * 128u + (uint32_t)((((cg >> 2) + 1) ^ (br & 7)) * 16), a[4], a[5], a[6], a[7]);
+          ld_block_v4(xb + (uint32_t)br * 128u + (uint32_t)(((cg >> 2) ^ (br & 7)) * 16), a[0], a[1], a[2], a[3]);
+          ld_block_v4(xb + (uint32_t)br * 128u + (uint32_t)((((cg >> 2) + 1) ^ (br & 7)) * 16), a[4], a[5], a[6], a[7]);
           if (t < s.T) {
             const int64_t col = n0 + c + cg;
             for (int j = 0; j < s.k; ++j) {

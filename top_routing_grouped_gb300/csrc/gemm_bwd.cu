@@ -22,11 +22,14 @@
 #include <cuda_bf16.h>
 
 #include "gemm_tc.h"
+#include "bwd_common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
 namespace moe {
 namespace {
+
+using namespace bwd;
 
 constexpr int kBK = 64;
 constexpr int kStages = 4;
@@ -35,7 +38,6 @@ constexpr int kTN = 256;  // tile columns (N)
 constexpr int kABytes = kTM * kBK * 2;
 constexpr int kBBytes = kTN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kBoxBytes = 64 * kBK * 2;  // one 64 x 64 MN-major box
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiThreads = 256;  // 8 warps: two per TMEM lane quarter, one per 128-column half
@@ -56,46 +58,12 @@ constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr size_t kSmemBytes =
     1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kOutBlockBytes + sizeof(Ctl);
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 __host__ __device__ constexpr bool a_mn(int kind) { return kind == kBwdDW13 || kind == kBwdDW2; }
 __host__ __device__ constexpr bool k_grouped(int kind) { return kind == kBwdDW13 || kind == kBwdDW2; }
 
-__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(kBoxBytes >> 4) << 16;  // leading: next 64-wide MN block
-  d |= (uint64_t)(1024 >> 4) << 32;       // stride: next 8 K rows
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
 
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
-__device__ __forceinline__ void unpack8(uint4 raw, float* f) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __bfloat1622float2(h[i]);
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
-  }
-}
 
 __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
@@ -464,10 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (blk_valid) {
             if (lane == 0) bulk_wait_read_all();  // the previous store has read the block
             __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_shared_v4(ob + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16), v[4 * j], v[4 * j + 1],
-                           v[4 * j + 2], v[4 * j + 3]);
+            stage_row32(ob, lane, v);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {

@@ -21,11 +21,14 @@
 #include <cuda_bf16.h>
 
 #include "gemm_bwd.h"
+#include "bwd_common.cuh"
 #include "gemm_tc.h"
 #include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace bwd;
 
 constexpr int kBK = 64;
 constexpr int kStages = 6;
@@ -33,7 +36,6 @@ constexpr int kRowsPerCta = 128;
 constexpr int kMmaM = 256;  // both CTAs
 constexpr int kMmaN = 256;
 constexpr int kABytes = kRowsPerCta * kBK * 2;  // 16 KB
-constexpr int kBoxBytes = 64 * kBK * 2;         // one 64 x 64 MN-major box
 constexpr int kBHalfBytes = 2 * kBoxBytes;      // 128 of the 256 columns
 constexpr int kStageBytes = kABytes + kBHalfBytes;
 constexpr int kAccCols = kMmaN;
@@ -58,30 +60,8 @@ struct Ctl2 {
 constexpr int kXposeBytes = 32 * 32 * 4;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kXposeBytes + sizeof(Ctl2);
 
-__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(kBoxBytes >> 4) << 16;  // leading: next 64-wide MN block
-  d |= (uint64_t)(1024 >> 4) << 32;       // stride: next 8 K rows
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
 
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
-__device__ __forceinline__ void unpack8(uint4 raw, float* f) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __bfloat1622float2(h[i]);
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
-  }
-}
 
 // The dH epilogue in the coalesced layout: lane l works on row 8 i + l / 4 (i = 0..3) of
 // the warp's 32 and on the 8 columns 8 (l % 4) .. of the 32-column chunk; these are the
@@ -90,13 +70,7 @@ struct DhIn {
   uint4 h[4], a[4], b[4];
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&f)[4]) {
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(addr) : "memory");
-}
 
 __device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
   ctl->abort = 1;
@@ -310,10 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld_32cols(t_row + c, v);
           ptx::tmem_ld_wait();
           // row `lane` of the block: its 16-byte chunk j at j ^ (lane % 8)
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(xb + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16), v[4 * j], v[4 * j + 1],
-                         v[4 * j + 2], v[4 * j + 3]);
+          stage_row32(xb, lane, v);
           __syncwarp();
           // each row group's operands are replaced by the next chunk's as soon as they are used
           const bool has_next = n0 + c + 32 < F && c + 32 < c_beg + kMmaN / 2;
@@ -321,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) {
             const int br = 8 * i + (lane >> 2);  // row within the block
             float dh[8];
-            ld_shared_v4(xb + (uint32_t)br * 128u + (uint32_t)((((cg >> 2)) ^ (br & 7)) * 16), *reinterpret_cast<float(*)[4]>(dh));
-            ld_shared_v4(xb + (uint32_t)br * 128u + (uint32_t)((((cg >> 2) + 1) ^ (br & 7)) * 16),
-                         *reinterpret_cast<float(*)[4]>(dh + 4));
+            ld_block_v4(xb + (uint32_t)br * 128u + (uint32_t)(((cg >> 2) ^ (br & 7)) * 16), dh[0], dh[1], dh[2], dh[3]);
+            ld_block_v4(xb + (uint32_t)br * 128u + (uint32_t)((((cg >> 2) + 1) ^ (br & 7)) * 16), dh[4], dh[5], dh[6],
+                         dh[7]);
             if (rv[i]) {
               float hv[8], av[8], bv[8];
               unpack8(in.h[i], hv);

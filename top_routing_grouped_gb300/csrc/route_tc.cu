@@ -7,8 +7,9 @@
 // layer streams x once (2 bytes per element against 2E flops), so it is bound by HBM, not by
 // the MMA; the tensor cores only keep the E dot products per token off the SIMT pipes.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
-// warps 2..5 epilogue (warp w reads TMEM lanes 32*(w%4)..: rows of its 32 tokens).
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
+// warps 2..9 epilogue, two per TMEM lane quarter (warp w reads lanes 32*(w%4)..: rows of its
+// 32 tokens), one for each half of the experts; each token is finished by a pair of threads.
 // Waits are bounded as in the expert GEMMs; if one runs out the block still finishes its
 // epilogue on zero logits (valid routing, status MOE_ERR_TIMEOUT) so no barrier is left open.
 #include <cuda.h>
@@ -24,7 +25,8 @@ namespace moe {
 namespace {
 
 constexpr int kBK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;  // warps 2..9
 constexpr int kMaxStages = 8;
 constexpr int kXBytes = kRouteBlock * kBK * 2;  // 16 KB
 constexpr int kMaxAcc = 4;                       // TMEM accumulators the K loop may use
@@ -43,7 +45,7 @@ struct RouteCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int vote[4];
+  int vote[8];
 };
 
 struct RouteGeom {
@@ -58,6 +60,13 @@ struct RouteGeom {
   uint32_t tmem_cols;
   size_t smem;      // dynamic shared memory
 };
+
+// The two threads of a token exchange their top-k values (kMaxTopK floats each), their parts
+// of the softmax denominator and their marked-expert bitmasks (8 words each).
+constexpr int xchg_bytes() { return 2 * kRouteBlock * (kMaxTopK + 1 + 8) * 4; }
+
+// Experts of half h of the columns: 16-column chunks [0, hc) and [hc, chunks).
+__host__ __device__ inline int expert_half_split(int e_pad) { return 16 * ((e_pad / 16 + 1) / 2); }
 
 RouteGeom route_geom(const Shape& s, int num_sms) {
   RouteGeom g;
@@ -79,7 +88,8 @@ RouteGeom route_geom(const Shape& s, int num_sms) {
   if (g.stages > kMaxStages) g.stages = kMaxStages;
   if (g.stages > g.kb_per) g.stages = g.kb_per;
   if (g.stages < 2) g.stages = 2;
-  const int zs = kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4;  // logits, then route_finish's masks
+  // logits, then the masks and per-row floats of the finish, then its pair exchange
+  const int zs = kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4 + xchg_bytes();
   g.body_bytes = g.stages * g.stage_bytes > zs ? g.stages * g.stage_bytes : zs;
   g.body_bytes = (g.body_bytes + 1023) / 1024 * 1024;
   // The tensor core's fp32 accumulation chain over K = d loses more than a SIMT sum; K-block
@@ -107,7 +117,246 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]
       : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+// Called by the 256 epilogue threads once z_s[r * ldz + e] holds the finished logits of the
+// block's token r (ldz odd): thread (r, h) owns the experts [e_lo, e_hi) of half h.  Same
+// results as route_finish (route_common.cuh), with the per-token work split over two threads:
+//   1. each thread keeps the KS largest values of its half (max/min network); the pair swaps
+//      lists through shared memory and each merges the other's into its own, so both hold
+//      the KS largest of the row (the same multiset, in the same descending order);
+//   2. each thread sums exp(z - max) over its half and marks its experts at or above the k-th
+//      value; the half-0 thread adds the two sums (half 0 first) and assigns the slots over
+//      both halves' marks in ascending expert order (ties: lower index first), then writes the
+//      gates, indices and the block's bitmasks;
+//   3. ranks from the bitmasks; per-block counts; per-expert sums of p over the block's rows
+//      by the eight warps (a lane adds rows lane, +32, +64, +96 in that order, then a fixed
+//      butterfly).
+template <int KS>
+__device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo,
+                                                int e_hi, float* z_s, int ldz, uint32_t* mask_s, int bar_id) {
+  const int E = s.E, k = s.k;
+  const int tid = h * kRouteBlock + r;
+  const int64_t t = (int64_t)blk * kRouteBlock + r;
+  const bool valid = t < s.T;
+  float* m_s = reinterpret_cast<float*>(mask_s + 4 * E);
+  float* inv_s = m_s + kRouteBlock;
+  float* xbv = inv_s + kRouteBlock;                                         // [2][128][kMaxTopK]
+  float* xsum = xbv + 2 * kRouteBlock * kMaxTopK;                           // [2][128]
+  uint32_t* xtake = reinterpret_cast<uint32_t*>(xsum + 2 * kRouteBlock);   // [2][128][8]
+  for (int i = tid; i < 4 * E; i += kEpiThreads) mask_s[i] = 0u;
+  const uint32_t zr = static_cast<uint32_t>(__cvta_generic_to_shared(z_s + r * ldz));
+
+  // pass 1: the KS largest values of this half (fmaxf(z, -inf) ranks a NaN as -inf)
+  float bv[KS];
+#pragma unroll
+  for (int j = 0; j < KS; ++j) bv[j] = -INFINITY;
+  bool nan_seen = false;
+  if (valid) {
+    for (int e0 = e_lo; e0 < e_hi; e0 += 8) {
+      float z8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) z8[u] = e0 + u < e_hi ? ld_shared_f32(zr + 4u * (uint32_t)(e0 + u)) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (s.keep_logits && e0 + u < e_hi) ws.logits[t * E + e0 + u] = z8[u];
+        nan_seen |= (z8[u] != z8[u]);
+        const float v = fmaxf(z8[u], -INFINITY);
+#pragma unroll
+        for (int j = KS - 1; j > 0; --j) bv[j] = fmaxf(bv[j], fminf(v, bv[j - 1]));
+        bv[0] = fmaxf(bv[0], v);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KS; ++j) xbv[tid * kMaxTopK + j] = bv[j];
+  named_barrier(bar_id, kEpiThreads);
+  // merge the other half's list into this one
+#pragma unroll
+  for (int i = 0; i < KS; ++i) {
+    const float v = xbv[((1 - h) * kRouteBlock + r) * kMaxTopK + i];
+#pragma unroll
+    for (int j = KS - 1; j > 0; --j) bv[j] = fmaxf(bv[j], fminf(v, bv[j - 1]));
+    bv[0] = fmaxf(bv[0], v);
+  }
+  if (nan_seen) record_error(ws, MOE_ERR_INTERNAL, 0x100u);
+  const float m = bv[0];
+  float thr = INFINITY;  // the k-th value: the least of the first k
+#pragma unroll
+  for (int j = 0; j < KS; ++j)
+    if (j < k) thr = fminf(thr, bv[j]);
+  int eq_left = k;  // slots open for logits equal to the k-th value
+#pragma unroll
+  for (int j = 0; j < KS; ++j) eq_left -= (j < k && bv[j] > thr) ? 1 : 0;
+
+  // pass 2: this half's part of the softmax denominator and its marked experts
+  uint32_t* my_take = xtake + tid * 8;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) my_take[w] = 0u;
+  float sum_h = 0.f;
+  if (valid) {
+    uint32_t cur = 0u;
+    int cw = e_lo >> 5;
+    for (int e0 = e_lo; e0 < e_hi; e0 += 4) {
+      float v4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v4[u] = e0 + u < e_hi ? fmaxf(ld_shared_f32(zr + 4u * (uint32_t)(e0 + u)), -INFINITY) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u;
+        if (e >= e_hi) break;
+        if ((e >> 5) != cw) {
+          my_take[cw] = cur;
+          cur = 0u;
+          cw = e >> 5;
+        }
+        sum_h += expf(v4[u] - m);
+        cur |= (v4[u] >= thr ? 1u : 0u) << (e & 31);
+      }
+    }
+    if (e_hi > e_lo) my_take[cw] = cur;
+  }
+  xsum[tid] = sum_h;
+  named_barrier(bar_id, kEpiThreads);
+
+  int bi[KS];
+#pragma unroll
+  for (int j = 0; j < KS; ++j) bi[j] = -1;
+  if (h == 0) {
+    float sum = 1.f;
+    if (valid) {
+      sum = xsum[r] + xsum[kRouteBlock + r];
+      uint32_t filled = 0u;
+      const uint32_t* t0w = xtake + r * 8;
+      const uint32_t* t1w = xtake + (kRouteBlock + r) * 8;
+      for (int w = 0; w < (E + 31) / 32; ++w) {
+        uint32_t take = t0w[w] | t1w[w];
+        while (take) {
+          const int e = w * 32 + __ffs(take) - 1;
+          take &= take - 1u;
+          const float v = fmaxf(ld_shared_f32(zr + 4u * (uint32_t)e), -INFINITY);
+          if (v == thr) {
+            if (eq_left == 0) continue;
+            --eq_left;
+          }
+          int pos0 = 0;
+#pragma unroll
+          for (int j = 0; j < KS; ++j) pos0 += (j < k && bv[j] > v) ? 1 : 0;
+          const int pos = __ffs(~filled & (0xffffffffu << pos0)) - 1;
+          if (pos >= 0 && pos < k) {
+            filled |= 1u << pos;
+#pragma unroll
+            for (int j = 0; j < KS; ++j)
+              if (j == pos) bi[j] = e;
+          }
+        }
+      }
+      // every slot is filled by construction; should one not be, report it and give it the
+      // lowest unused expert so that every later index stays in range and distinct
+      if (filled != (1u << k) - 1u) {
+        record_error(ws, MOE_ERR_INTERNAL, 0x101u);
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          if (j < k && bi[j] < 0) {
+            for (int e = 0; e < E; ++e) {
+              bool used = false;
+#pragma unroll
+              for (int q = 0; q < KS; ++q) used |= (q < k && bi[q] == e);
+              if (!used) {
+                bi[j] = e;
+                break;
+              }
+            }
+          }
+        }
+      }
+      float gate[KS];
+      float chosen = 0.f;  // sum of the chosen gates, in slot order (renormalised variant)
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        gate[j] = j < k ? expf(fmaxf(ld_shared_f32(zr + 4u * (uint32_t)bi[j]), -INFINITY) - m) / sum : 0.f;
+        chosen += gate[j];
+      }
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        if (j < k) {
+          const int e = bi[j];
+          ws.topk_idx[t * k + j] = e;
+          ws.topk_gate[t * k + j] = s.renorm ? gate[j] / chosen : gate[j];
+          atomicOr(&mask_s[e * 4 + (r >> 5)], 1u << (r & 31));
+        }
+      }
+    }
+    m_s[r] = valid ? m : 0.f;
+    inv_s[r] = 1.f / sum;
+  }
+  named_barrier(bar_id, kEpiThreads);
+
+  if (h == 0 && valid) {
+    const uint32_t below = (1u << (r & 31)) - 1u;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      if (j < k) {
+        const uint32_t* mk = mask_s + bi[j] * 4;
+        int rank = __popc(mk[r >> 5] & below);
+        for (int wd = 0; wd < (r >> 5); ++wd) rank += __popc(mk[wd]);
+        ws.local_rank[t * k + j] = rank;
+      }
+    }
+  }
+  for (int e = tid; e < E; e += kEpiThreads) {
+    const uint32_t* mk = mask_s + e * 4;
+    ws.blk_cnt[(int64_t)blk * E + e] = __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
+  }
+  // per-expert sums of p = exp(z - max) / sum over the block's rows (rows past T add 0)
+  const int w8 = tid >> 5, lane = tid & 31;
+  const int64_t t_base = (int64_t)blk * kRouteBlock;
+  float mrow[4], inv[4];
+  bool vrow[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    mrow[j] = m_s[lane + 32 * j];
+    inv[j] = inv_s[lane + 32 * j];
+    vrow[j] = t_base + lane + 32 * j < s.T;
+  }
+  const uint32_t zc = static_cast<uint32_t>(__cvta_generic_to_shared(z_s + lane * ldz));
+  for (int e0 = 4 * w8; e0 < E; e0 += 32) {
+    float zz[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        zz[j][u] = e0 + u < E ? ld_shared_f32(zc + 4u * (uint32_t)(32 * j * ldz + e0 + u)) : 0.f;
+    float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int row = lane + 32 * j;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float p = vrow[j] ? expf(fmaxf(zz[j][u], -INFINITY) - mrow[j]) * inv[j] : 0.f;
+        if (s.training && vrow[j] && e0 + u < E) ws.probs[(t_base + row) * E + e0 + u] = p;
+        ps[u] += p;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ps[u] += __shfl_xor_sync(0xffffffffu, ps[u], off);
+    if (lane == 0)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (e0 + u < E) ws.blk_psum[(int64_t)blk * E + e0 + u] = ps[u];
+  }
+}
+
+__device__ __forceinline__ void route_finish2(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo, int e_hi,
+                                              float* z_s, int ldz, uint32_t* mask_s, int bar_id) {
+  if (s.k <= 2) route_finish2_k<2>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  else if (s.k <= 4) route_finish2_k<4>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  else if (s.k <= 8) route_finish2_k<8>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  else route_finish2_k<kMaxTopK>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                              const __grid_constant__ CUtensorMap tmW, Shape s, Ws ws,
                                                              Weights w, RouteGeom g, int64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -208,15 +457,22 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
   } else {
     // ------------------------------------------------------------------ epilogue, part 1:
     // this CTA's partial logits (sum of its accumulators) into z_s (leader; finished with
-    // bias and temperature when the CTA is alone) or into the leader's receive buffer
+    // bias and temperature when the CTA is alone) or into the leader's receive buffer; the
+    // two warps of a lane quarter take the two halves of the expert columns
+    const int ew = warp - 2;
     const int q = warp & 3;
+    const int h = ew >> 2;
     const int r = q * 32 + lane;  // token row of this block
-    for (int e = r; e < g.e_pad; e += kRouteBlock) bias_s[e] = (s.has_bias && e < s.E) ? w.bias[e] : 0.f;
+    const int eh = expert_half_split(g.e_pad);
+    const int c_lo = h == 0 ? 0 : eh, c_hi = h == 0 ? eh : g.e_pad;  // this warp's 16-column chunks
+    for (int e = ew * 32 + lane; e < g.e_pad; e += kEpiThreads) bias_s[e] = (s.has_bias && e < s.E) ? w.bias[e] : 0.f;
     bool ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull), 0u, timeout_ns, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    if (lane == 0) ctl->vote[q] = ok ? 1 : 0;
-    named_barrier(2, kRouteBlock);
-    const bool all_ok = ctl->vote[0] && ctl->vote[1] && ctl->vote[2] && ctl->vote[3];
+    if (lane == 0) ctl->vote[ew] = ok ? 1 : 0;
+    named_barrier(2, kEpiThreads);
+    bool all_ok = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) all_ok = all_ok && ctl->vote[i];
     float* z_s = reinterpret_cast<float*>(body);
     const int ldz = s.E + 1;
     const bool finish_here = g.split == 1;
@@ -228,7 +484,7 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
       const uint32_t z_row = ptx::smem_u32(z_s + r * ldz);
       const uint32_t b_base = ptx::smem_u32(bias_s);
       const int used = kblocks < g.n_acc ? kblocks : g.n_acc;  // accumulators that were written
-      for (int c = 0; c < g.e_pad; c += 16) {
+      for (int c = c_lo; c < c_hi; c += 16) {
         // every accumulator's 16 columns in flight at once, and the bias beside them
         uint32_t v[kMaxAcc][16];
 #pragma unroll
@@ -259,8 +515,8 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
         }
       }
     } else {
-      if (lane == 0 && q == 0) record_error(ws, MOE_ERR_TIMEOUT, 0x620u);
-      for (int e = 0; e < s.E; ++e) {
+      if (lane == 0 && ew == 0) record_error(ws, MOE_ERR_TIMEOUT, 0x620u);
+      for (int e = c_lo; e < c_hi && e < s.E; ++e) {
         if (rank == 0) z_s[r * ldz + e] = finish_here ? finish_logit(0.f, bias_s[e], s.tau) : 0.f;
         else ptx::st_cluster_u32(recv_remote + 4u * (uint32_t)e, 0u);
       }
@@ -272,9 +528,14 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
   if (rank == 0 && warp >= 2) {
     // ------------------------------------------------------------------ epilogue, part 2
     // (leader): add the other CTAs' partials in rank order, bias, temperature; then the
-    // softmax / top-k / counting of route_finish
+    // softmax / top-k / counting, two threads per token
+    const int ew = warp - 2;
     const int q = warp & 3;
+    const int h = ew >> 2;
     const int r = q * 32 + lane;
+    const int eh = expert_half_split(g.e_pad);
+    const int e_lo = h == 0 ? 0 : eh;
+    const int e_hi = h == 0 ? (eh < s.E ? eh : s.E) : s.E;
     float* z_s = reinterpret_cast<float*>(body);
     uint32_t* mask_s = reinterpret_cast<uint32_t*>(z_s + kRouteBlock * (s.E + 1));
     const int ldz = s.E + 1;
@@ -282,8 +543,8 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
       const uint32_t z_row = ptx::smem_u32(z_s + r * ldz);
       const uint32_t r_row = ptx::smem_u32(recv + r * ldz);
       const uint32_t b_base = ptx::smem_u32(bias_s);
-      for (int c = 0; c < s.E; c += 16) {
-        const int n = s.E - c < 16 ? s.E - c : 16;
+      for (int c = e_lo; c < e_hi; c += 16) {
+        const int n = e_hi - c < 16 ? e_hi - c : 16;
         float z[16], b[16];
 #pragma unroll
         for (int i = 0; i < 16; i += 4) ld_shared_v4(b_base + 4u * (uint32_t)(c + i), b[i], b[i + 1], b[i + 2], b[i + 3]);
@@ -299,8 +560,9 @@ __global__ void __launch_bounds__(kThreads) route_tc_kernel(const __grid_constan
         for (int i = 0; i < 16; ++i)
           if (i < n) st_shared_f32(z_row + 4u * (uint32_t)(c + i), finish_logit(z[i], b[i], s.tau));
       }
+      named_barrier(1, kEpiThreads);  // the other half's finished logits are in z_s too
     }
-    route_finish(s, ws, blk, r, z_s, ldz, mask_s, /*bar_id=*/1);
+    route_finish2(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, /*bar_id=*/1);
   }
 
   __syncthreads();

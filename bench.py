@@ -495,6 +495,29 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status {st} after the back-to-back kernel timing")
 
+    # timed region 4: the forward captured once into a CUDA graph and replayed K times (the
+    # same flush between steps, outside the events)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        plan.forward(*targs)
+    for _ in range(3):
+        graph.replay()
+    gev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    gev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        gev_s[i].record(stream)
+        graph.replay()
+        gev_e[i].record(stream)
+    torch.cuda.synchronize()
+    st = plan.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the graph replays")
+    graph_ms = sum(gev_s[i].elapsed_time(gev_e[i]) for i in range(K)) / K
+    graph_max_ms = reduce_max(graph_ms * K, "cuda")
+    del graph
+
     # end to end through the host-buffer entry point: pinned x in, pinned y out, every step
     e2e = None
     if not args.no_e2e:
@@ -547,6 +570,8 @@ def main():
                          "unit": "TFLOP/s", "frac": g1_tflops / pk["bf16"], "traffic": traffic,
                          "peak_source": f"{pk['src']} bf16 burst", "frac_of_sustained": g1_tflops / pk["bf16_sust"],
                          "algorithmic": f"4*N*d*F = {g1_flops} FLOP per launch (N = T*k = {shape.N} rows)"},
+            "graph": {"ms_per_step": graph_max_ms / K, "tokens_per_s": throughput(shape.T, K, world, graph_max_ms),
+                      "from": "one forward captured into a CUDA graph, K replays (timed region 4)"},
             "e2e": e2e,
             "gpu_launches": len(STAGES) * K,
             "ms_per_step_with_stage_events": staged_step_ms,

@@ -105,7 +105,7 @@ typedef struct {
   float* logits;           /* [T,E] router logits, or NULL unless MOE_FLAG_KEEP_LOGITS */
   void* xp;                /* [N,d] act dtype: x rows in dispatch order */
   void* h;                 /* [N,F] act dtype: SwiGLU hidden rows */
-  void* yslot;             /* [T*k,d] act dtype: gate * expert output, token-slot order */
+  void* yp;                /* [N,d] act dtype: row p = gate * expert output of row p (expert order) */
 } moe_views;
 
 /* Build a plan for one layer shape (host only; no device work).  Validates the config

@@ -92,10 +92,8 @@ WsLayout ws_layout(const Shape& s) {
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
   L.blk_base = take(nb * E * 4);
-  L.grp_expert = take((size_t)s.max_groups * 4);
-  L.grp_mtile0 = take((size_t)s.max_groups * 4);
-  L.grp_mpre = take(((size_t)s.max_groups + 1) * 4);
-  L.grp_ppre = take(((size_t)s.max_groups + 1) * 4);
+  L.mt_desc = take((size_t)s.max_groups * moe::kGroupM * 16);
+  L.pr_desc = take((size_t)s.max_groups * (moe::kGroupM / 2) * 16);
   L.perm_src = take(N * 4);
   L.perm_slot = take(N * 4);
   L.gate_perm = take(N * 4);
@@ -103,7 +101,7 @@ WsLayout ws_layout(const Shape& s) {
   L.logits = s.keep_logits ? take((size_t)s.T * E * 4) : 0;
   L.xp = take(N * (size_t)s.d * esz);
   L.h = take(N * (size_t)s.F * esz);
-  L.yslot = take(N * (size_t)s.d * esz);
+  L.yp = take(N * (size_t)s.d * esz);
   if (s.training) {
     const size_t nt = 2 * (((size_t)s.F + 255) / 256), chunks = (size_t)dwr_chunks(s);
     L.a1 = take(N * (size_t)s.F * 2);
@@ -138,10 +136,8 @@ Ws ws_bind(const Shape& s, void* base) {
   w.counts = reinterpret_cast<int32_t*>(b + L.counts);
   w.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
   w.blk_base = reinterpret_cast<int32_t*>(b + L.blk_base);
-  w.grp_expert = reinterpret_cast<int32_t*>(b + L.grp_expert);
-  w.grp_mtile0 = reinterpret_cast<int32_t*>(b + L.grp_mtile0);
-  w.grp_mpre = reinterpret_cast<int32_t*>(b + L.grp_mpre);
-  w.grp_ppre = reinterpret_cast<int32_t*>(b + L.grp_ppre);
+  w.mt_desc = reinterpret_cast<int4*>(b + L.mt_desc);
+  w.pr_desc = reinterpret_cast<int4*>(b + L.pr_desc);
   w.perm_src = reinterpret_cast<int32_t*>(b + L.perm_src);
   w.perm_slot = reinterpret_cast<int32_t*>(b + L.perm_slot);
   w.gate_perm = reinterpret_cast<float*>(b + L.gate_perm);
@@ -149,7 +145,7 @@ Ws ws_bind(const Shape& s, void* base) {
   w.logits = s.keep_logits ? reinterpret_cast<float*>(b + L.logits) : nullptr;
   w.xp = b + L.xp;
   w.h = b + L.h;
-  w.yslot = b + L.yslot;
+  w.yp = b + L.yp;
   if (s.training) {
     w.a1 = b + L.a1;
     w.a3 = b + L.a3;
@@ -466,7 +462,7 @@ moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* v) {
   v->logits = w.logits;
   v->xp = w.xp;
   v->h = w.h;
-  v->yslot = w.yslot;
+  v->yp = w.yp;
   return MOE_OK;
 }
 

@@ -1,8 +1,9 @@
-// combine.cu -- y[t] = sum_{j<k} Yslot[t*k + j], in j order, fp32 accumulation.
+// combine.cu -- y[t] = sum_{j<k} Yp[slot_pos[t*k + j]], in j order, fp32 accumulation.
 //
 // After "Distributed Training Part 4 ... MoE + Expert Parallelism" (jesamkim ai-tech-blog),
 // §3 output formula y = sum_{i in TopK} G(x)_i E_i(x) (the gate factor is already applied
-// by the down-projection epilogue) and §4 Combine (expert outputs return to their token).
+// by the down-projection epilogue) and §4 Combine (expert outputs return to their token:
+// Yp holds them in expert order, slot_pos[t*k + j] is the row of token t's j-th choice).
 // A fixed summation order keeps y bit-reproducible (no float atomics).
 #include <cuda_bf16.h>
 
@@ -17,8 +18,8 @@ template <bool kOutBf16>
 __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws ws, Weights w) {
   const int vec_per_row = s.d / 8;
   const int64_t total = s.T * (int64_t)vec_per_row;
-  const int4* ys = reinterpret_cast<const int4*>(ws.yslot);
-  pdl_wait();  // per-slot outputs of the down-projection
+  const int4* ys = reinterpret_cast<const int4*>(ws.yp);
+  pdl_wait();  // the down-projection's rows
   pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * kCombThreads) {
@@ -28,7 +29,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws 
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
     for (int j = 0; j < s.k; ++j) {
-      int4 raw = __ldcs(ys + (t * s.k + j) * vec_per_row + v);
+      const int64_t row = __ldg(&ws.slot_pos[t * s.k + j]);
+      int4 raw = __ldcs(ys + row * vec_per_row + v);
       const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -56,7 +58,7 @@ template <bool kOutBf16>
 __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws ws, Weights w) {
   const int vec_per_row = s.d / 4;
   const int64_t total = s.T * (int64_t)vec_per_row;
-  const float4* ys = reinterpret_cast<const float4*>(ws.yslot);
+  const float4* ys = reinterpret_cast<const float4*>(ws.yp);
   pdl_wait();
   pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
     const int v = (int)(i % vec_per_row);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < s.k; ++j) {
-      const float4 f = ys[(t * s.k + j) * vec_per_row + v];
+      const float4 f = ys[(int64_t)__ldg(&ws.slot_pos[t * s.k + j]) * vec_per_row + v];
       acc.x += f.x;
       acc.y += f.y;
       acc.z += f.z;

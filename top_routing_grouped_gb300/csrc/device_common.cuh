@@ -85,23 +85,16 @@ struct TileInfo {
 // m-tiles of one expert; inside a group the m-tile index runs fastest, so CTAs that run
 // at the same time share the same weight n-tile (read once from HBM, then from L2).
 // Group g owns tiles [n_tiles * mpre[g], n_tiles * mpre[g+1]).
-__device__ __forceinline__ TileInfo decode_tile(const Ws& ws, int ngroups, int n_tiles, int tile) {
-  const int q = tile / n_tiles;
-  int lo = 0, hi = ngroups - 1;  // largest g with mpre[g] <= q
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&ws.grp_mpre[mid]) <= q) lo = mid; else hi = mid - 1;
-  }
-  const int g = lo;
-  const int m_begin = __ldg(&ws.grp_mpre[g]);
-  const int gm = __ldg(&ws.grp_mpre[g + 1]) - m_begin;
-  const int local = tile - n_tiles * m_begin;
+// The group is found from the descriptor of entry tile / n_tiles (one load).
+__device__ __forceinline__ TileInfo decode_tile(const Ws& ws, int n_tiles, int tile) {
+  const int4 g = __ldg(&ws.mt_desc[tile / n_tiles]);
+  const int gm = g.x >> 20;
+  const int local = tile - n_tiles * g.y;
   TileInfo ti;
-  ti.e = __ldg(&ws.grp_expert[g]);
+  ti.e = g.x & 0xFFFFF;
   ti.n_idx = local / gm;
-  const int mt = __ldg(&ws.grp_mtile0[g]) + local % gm;
-  ti.row0 = __ldg(&ws.offsets[ti.e]) + mt * kTileM;
-  const int rem = __ldg(&ws.counts[ti.e]) - mt * kTileM;
+  ti.row0 = g.z + (local % gm) * kTileM;
+  const int rem = g.w - ti.row0;
   ti.rows = rem < kTileM ? rem : kTileM;
   return ti;
 }
@@ -110,23 +103,15 @@ __device__ __forceinline__ TileInfo decode_tile(const Ws& ws, int ngroups, int n
 // is two consecutive m-tiles of one scheduling group (the second may not exist: rows <= 0)
 // times one n-tile; group g owns pair tiles [n_tiles * ppre[g], n_tiles * ppre[g+1]) and
 // inside a group the pair index runs fastest.
-__device__ __forceinline__ TileInfo decode_pair_tile(const Ws& ws, int ngroups, int n_tiles, int tile, int rank) {
-  const int q = tile / n_tiles;
-  int lo = 0, hi = ngroups - 1;  // largest g with ppre[g] <= q
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&ws.grp_ppre[mid]) <= q) lo = mid; else hi = mid - 1;
-  }
-  const int g = lo;
-  const int p_begin = __ldg(&ws.grp_ppre[g]);
-  const int gp = __ldg(&ws.grp_ppre[g + 1]) - p_begin;
-  const int local = tile - n_tiles * p_begin;
+__device__ __forceinline__ TileInfo decode_pair_tile(const Ws& ws, int n_tiles, int tile, int rank) {
+  const int4 g = __ldg(&ws.pr_desc[tile / n_tiles]);
+  const int gp = g.x >> 20;
+  const int local = tile - n_tiles * g.y;
   TileInfo ti;
-  ti.e = __ldg(&ws.grp_expert[g]);
+  ti.e = g.x & 0xFFFFF;
   ti.n_idx = local / gp;
-  const int mt = __ldg(&ws.grp_mtile0[g]) + 2 * (local % gp) + rank;
-  ti.row0 = __ldg(&ws.offsets[ti.e]) + mt * kTileM;
-  const int rem = __ldg(&ws.counts[ti.e]) - mt * kTileM;
+  ti.row0 = g.z + (2 * (local % gp) + rank) * kTileM;
+  const int rem = g.w - ti.row0;
   ti.rows = rem < kTileM ? rem : kTileM;  // <= 0: no such m-tile (odd group), nothing stored
   return ti;
 }

@@ -117,10 +117,10 @@ __device__ __forceinline__ void kind_dims(const Shape& s, int& M, int& N, int& K
 }
 
 template <int kKind>
-__device__ __forceinline__ BTile decode(const BwdArgs& a, int tile, int ngroups, int n_tiles, int m_tiles) {
+__device__ __forceinline__ BTile decode(const BwdArgs& a, int tile, int n_tiles, int m_tiles) {
   BTile b{};
   if (!k_grouped(kKind)) {
-    const TileInfo ti = decode_tile(a.ws, ngroups, n_tiles, tile);
+    const TileInfo ti = decode_tile(a.ws, n_tiles, tile);
     int M, N, K;
     kind_dims<kKind>(a.s, M, N, K);
     b.e = ti.e;
@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctl->abort;
   pdl_wait();
   pdl_launch_dependents();
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
   const int total = k_grouped(kKind) ? s.E * m_tiles * n_tiles : (int)ws.hdr[kHdrNumMTiles] * n_tiles;
   uint32_t issued = 0, issued_phase = 0;
 
@@ -201,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+        const BTile bt = decode<kKind>(args, tile, n_tiles, m_tiles);
         const int n0 = bt.n_idx * kTN;
         for (int kb = 0; kb < bt.kblocks; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+      const BTile bt = decode<kKind>(args, tile, n_tiles, m_tiles);
       ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, timeout_ns, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -316,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const BTile bt = decode<kKind>(args, tile, ngroups, n_tiles, m_tiles);
+      const BTile bt = decode<kKind>(args, tile, n_tiles, m_tiles);
       const bool valid = r < bt.rows;
       const int n0 = bt.n_idx * kTN;
       // dH: the row's h / a / b are requested a chunk ahead of their use, the first chunk

@@ -129,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();
   pdl_wait();  // the tile table and the A operand come from the previous kernels
   pdl_launch_dependents();
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
   int total = (int)ws.hdr[kHdrNumPairs] * n_tiles;
   if (ctl->peer_tmem_base != tmem) {  // a pair's accumulators must sit at the same TMEM address
     if (threadIdx.x == 0) record_error(ws, MOE_ERR_INTERNAL, 0x900u + kKind);
@@ -144,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = cid; tile < total && ok; tile += ncl) {
-        const TileInfo ti = decode_pair_tile(ws, ngroups, n_tiles, tile, (int)rank);
+        const TileInfo ti = decode_pair_tile(ws, n_tiles, tile, (int)rank);
         const int nb = ti.n_idx * kMmaN + (int)rank * (kMmaN / 2);  // this CTA's B columns
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
@@ -234,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = cid; tile < total; tile += ncl) {
-      const TileInfo ti = decode_pair_tile(ws, ngroups, n_tiles, tile, (int)rank);
+      const TileInfo ti = decode_pair_tile(ws, n_tiles, tile, (int)rank);
       const bool valid = r < ti.rows;
       const int n0 = ti.n_idx * kMmaN;
       const int64_t p = (int64_t)ti.row0 + r;

@@ -37,14 +37,13 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(Shape s, Ws ws,
   const Act* B3 = reinterpret_cast<const Act*>(w.w3);
   pdl_wait();  // tile table, permuted rows (or H) of the previous kernels
   pdl_launch_dependents();
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
   const int total = (int)ws.hdr[kHdrNumMTiles] * n_tiles;
 
   const int tid = threadIdx.x;
   const int tx = tid % 16, ty = tid / 16;  // 4 columns x 8 rows per thread
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const TileInfo ti = decode_tile(ws, ngroups, n_tiles, tile);
+    const TileInfo ti = decode_tile(ws, n_tiles, tile);
     const int n0 = ti.n_idx * kSimtBN;
     const int64_t wrow0 = (int64_t)ti.e * ncols;  // first weight row of this expert
     float acc[8][4], acc3[8][4];  // acc3: W3 products (GEMM1 only; unused otherwise)
@@ -112,16 +111,11 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(Shape s, Ws ws,
           store_act(ws.h, kBf16, p * s.F + c, hv);
         }
       } else {
-        const int64_t slot = ws.perm_slot[p];
         const float g = ws.gate_perm[p];
-        if (slot < 0 || slot >= s.N) {
-          record_error(ws, MOE_ERR_INTERNAL, 0x400u);
-          continue;
-        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int c = n0 + tx * 4 + j;
-          if (c < ncols) store_act(ws.yslot, kBf16, slot * s.d + c, g * acc[i][j]);
+          if (c < ncols) store_act(ws.yp, kBf16, p * s.d + c, g * acc[i][j]);
         }
       }
     }

@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctl->abort;
   pdl_wait();  // the tile table and the A operand come from the previous kernels
   pdl_launch_dependents();
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
   const int total = (int)ws.hdr[kHdrNumMTiles] * n_tiles;
 
   // fills issued by the producer whose landing nobody may have waited for (abort path)
@@ -128,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true, first = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(ws, ngroups, n_tiles, tile);
+        const TileInfo ti = decode_tile(ws, n_tiles, tile);
         const int brow = kMode == 1 ? ti.e * s.F + ti.n_idx * bn : ti.e * s.d + ti.n_idx * bn;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
@@ -214,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(ws, ngroups, n_tiles, tile);
+      const TileInfo ti = decode_tile(ws, n_tiles, tile);
       ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull[acc]), acc_phase, timeout_ns, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -267,23 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        int64_t slot = -1;
-        float gate = 0.f;
-        if (valid) {
-          slot = ws.perm_slot[p];
-          gate = ws.gate_perm[p];
-          if (slot < 0 || slot >= s.N) {
-            record_error(ws, MOE_ERR_INTERNAL, 0x520u);
-            slot = -1;
-          }
-        }
-        __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(ws.yslot) + slot * s.d + n0;
+        const float gate = valid ? ws.gate_perm[p] : 0.f;
+        __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(ws.yp) + p * s.d + n0;
 #pragma unroll 1
         for (int c = 0; c < kMmaN; c += 32) {
           uint32_t a[32];
           ptx::tmem_ld_32cols(t_row + c, a);
           ptx::tmem_ld_wait();
-          if (slot >= 0 && n0 + c < s.d) {
+          if (valid && n0 + c < s.d) {
             uint4* dst = reinterpret_cast<uint4*>(yrow + c);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {

@@ -11,8 +11,13 @@
 // so an SM pulls 32 KB per 64-deep K step instead of 48 KB and the ring holds 6 stages.
 // Both CTAs' loads signal the leader's "full" barrier; the leader's commits free the stage in
 // both CTAs (multicast arrive) and hand each CTA its 128 accumulator rows in its own TMEM.
-// The epilogue is the one-SM kernel's, per CTA; its warps release the accumulator to the
-// leader with a cluster-scope arrive.
+// The epilogue runs per CTA; its warps release the accumulator to the leader with a
+// cluster-scope arrive.  Mode 1 stores its H rows directly.  Mode 2 writes Yp in the same
+// expert-contiguous row order as its A operand, so each warp's 32 rows x 64 columns form one
+// tile of Yp: the warp stages it in shared memory (128-byte swizzle, double-buffered) and one
+// lane hands it to the TMA engine as a tiled store.  Only a warp block that crosses the end of
+// the expert's rows stores its valid rows directly (a tiled store would overwrite the next
+// expert's first rows).
 //
 // Waits are bounded (MOE_ERR_TIMEOUT, no trap); an abort raises the flag in both CTAs; the
 // pair meets at cluster barriers before TMEM is released.
@@ -26,7 +31,7 @@ namespace moe {
 namespace {
 
 constexpr int kBK = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 6;  // ring depth of mode 1; mode 2 gives one stage to its store staging
 constexpr int kRowsPerCta = 128;
 constexpr int kMmaM = 256;  // both CTAs
 constexpr int kMmaN = 256;
@@ -50,7 +55,19 @@ struct Ctl2 {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl2);
+// mode 2's store staging: per epilogue warp two blocks of 32 rows x 64 bf16 columns (128-byte
+// rows, 16-byte chunk j of row r at j ^ (r % 8): the TMA 128-byte swizzle), 1024-byte aligned
+constexpr int kStgBlockBytes = 32 * 128;
+constexpr int kStgBytes = kEpiWarps * 2 * kStgBlockBytes;
+
+template <int kMode>
+constexpr int ring_stages() { return kMode == 1 ? kStages : kStages - 1; }
+
+template <int kMode>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)ring_stages<kMode>() * kStageBytes + (kMode == 2 ? kStgBytes : 0) + sizeof(Ctl2);
+}
+static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -58,6 +75,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 __device__ __forceinline__ float silu(float a) { return silu_fast(a); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 2-D tiled TMA store of a staged block (x = column, y = row), as a bulk group of its own
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+// at most one of this thread's bulk groups still reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// all of this thread's bulk groups complete (their global writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
   ctl->abort = 1;
@@ -67,10 +101,13 @@ __device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
 template <int kMode, int kAccBufs>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB3, Shape s, Ws ws, int64_t timeout_ns, int stall) {
+                    const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmY, Shape s,
+                    Ws ws, int64_t timeout_ns, int stall) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl2* ctl = reinterpret_cast<Ctl2*>(stages + kStages * kStageBytes);
+  constexpr int kRing = ring_stages<kMode>();
+  uint8_t* stg_base = stages + kRing * kStageBytes;  // mode 2's store staging
+  Ctl2* ctl = reinterpret_cast<Ctl2*>(stg_base + (kMode == 2 ? kStgBytes : 0));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -85,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kblocks = K / kBK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kRing; ++i) {
       ptx::mbar_init(ptx::smem_u32(&ctl->full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&ctl->empty[i]), 1);
     }
@@ -102,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
     if (kMode == 1) ptx::tma_prefetch_desc(&tmB3);
+    if (kMode == 2) ptx::tma_prefetch_desc(&tmY);
   }
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive or load
   if (warp == 2) {
@@ -116,7 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();
   pdl_wait();  // the tile table and the A operand come from the previous kernels
   pdl_launch_dependents();
-  const int ngroups = (int)ws.hdr[kHdrNumGroups];
   int total = (int)ws.hdr[kHdrNumPairs] * n_tiles;
   if (ctl->peer_tmem_base != tmem) {  // a pair's accumulators must sit at the same TMEM address
     if (threadIdx.x == 0) record_error(ws, MOE_ERR_INTERNAL, 0x700u + kMode);
@@ -132,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, first = true;
       const CUtensorMap* bmap = (kMode == 1 && rank == 1) ? &tmB3 : &tmB;
       for (int tile = cid; tile < total && ok; tile += ncl) {
-        const TileInfo ti = decode_pair_tile(ws, ngroups, n_tiles, tile, (int)rank);
+        const TileInfo ti = decode_pair_tile(ws, n_tiles, tile, (int)rank);
         const int brow = kMode == 1 ? ti.e * s.F + ti.n_idx * bn : ti.e * s.d + ti.n_idx * bn + (int)rank * (kMmaN / 2);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, timeout_ns, abort_flag)) {
@@ -148,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_load_2d_pair(sa + kABytes, bmap, kb * kBK, brow, bar);
           }
           first = false;
-          if (++stage == kStages) {
+          if (++stage == kRing) {
             stage = 0;
             phase ^= 1u;
           }
@@ -187,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_bf16_pair(d_tmem, ptx::desc_kmajor_sw128(sa + ks * kMmaK * 2),
                                ptx::desc_kmajor_sw128(sb + ks * kMmaK * 2), idesc, (kb | ks) != 0 ? 1u : 0u);
           ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
-          if (++stage == kStages) {
+          if (++stage == kRing) {
             stage = 0;
             phase ^= 1u;
           }
@@ -209,11 +246,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const uint32_t stg = ptx::smem_u32(stg_base) + (uint32_t)(q * 2 * kStgBlockBytes);
+    int stg_buf = 0;  // the staging block this lane's next copy uses
+    (void)stg;
+    (void)stg_buf;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = cid; tile < total; tile += ncl) {
-      const TileInfo ti = decode_pair_tile(ws, ngroups, n_tiles, tile, (int)rank);
+      const TileInfo ti = decode_pair_tile(ws, n_tiles, tile, (int)rank);
       ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull[acc]), acc_phase, timeout_ns, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -265,34 +306,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        int64_t slot = -1;
-        float gate = 0.f;
-        if (valid) {
-          slot = ws.perm_slot[p];
-          gate = ws.gate_perm[p];
-          if (slot < 0 || slot >= s.N) {
-            record_error(ws, MOE_ERR_INTERNAL, 0x560u);
-            slot = -1;
-          }
-        }
-        __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(ws.yslot) + slot * s.d + n0;
+        const float gate = valid ? ws.gate_perm[p] : 0.f;
+        // rows of this warp's 32-row block that belong to the tile's expert: all 32 -> one
+        // tiled store per 64 columns; fewer -> each valid lane stores its own row piece
+        const int vw = ti.rows - q * 32;
+        __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(ws.yp) + p * s.d + n0;
 #pragma unroll 1
-        for (int c = 0; c < kMmaN; c += 32) {
-          uint32_t a[32];
+        for (int c = 0; c < kMmaN; c += 64) {
+          uint32_t a[32], b[32];
           ptx::tmem_ld_32cols(t_row + c, a);
+          ptx::tmem_ld_32cols(t_row + c + 32, b);
           ptx::tmem_ld_wait();
-          if (slot >= 0 && n0 + c < s.d) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+          if (vw > 0 && n0 + c < s.d) {  // warp-uniform
+            uint32_t pk[32];  // the row's 64 bf16 values
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+            for (int i = 0; i < 16; ++i) {
+              pk[i] = pack_bf16x2(gate * __uint_as_float(a[2 * i]), gate * __uint_as_float(a[2 * i + 1]));
+              pk[16 + i] = pack_bf16x2(gate * __uint_as_float(b[2 * i]), gate * __uint_as_float(b[2 * i + 1]));
+            }
+            if (vw >= 32) {
+              const uint32_t blk = stg + (uint32_t)(stg_buf * kStgBlockBytes);
+              if (lane == 0) bulk_wait_read_le1();  // the store issued from this block two chunks ago has read it
+              __syncwarp();
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int i = v * 8 + u * 2;
-                ow[u] = pack_bf16x2(gate * __uint_as_float(a[i]), gate * __uint_as_float(a[i + 1]));
-              }
-              dst[v] = o;
+              for (int j = 0; j < 8; ++j)
+                st_shared_v4(blk + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) * 16)), pk[4 * j], pk[4 * j + 1],
+                             pk[4 * j + 2], pk[4 * j + 3]);
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA engine
+              __syncwarp();
+              if (lane == 0) tma_store_2d(&tmY, n0 + c, ti.row0 + q * 32, blk);
+              stg_buf ^= 1;
+            } else if (lane < vw) {
+              uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
           }
         }
@@ -305,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (kMode == 2) bulk_wait_all();  // the tiled stores this lane issued have been written
     if (!ok && lane == 0) {
       record_error(ws, MOE_ERR_TIMEOUT, 0x570u + kMode);
       raise_abort(ctl, rank);
@@ -337,9 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int kMode, int kAccBufs>
-cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const Shape& s, const Ws& ws,
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const CUtensorMap& y,
+                        const Shape& s, const Ws& ws,
                         int num_sms, int64_t timeout_ns, bool stall, bool pdl, cudaStream_t st) {
   auto kern = gemm_tc2_kernel<kMode, kAccBufs>;
+  constexpr size_t kSmemBytes = smem_bytes<kMode>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   // as many pairs as can be resident at once (persistent loop over pair tiles)
@@ -360,7 +410,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtens
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0 && 2 * clusters < grid)
       grid = 2 * clusters;
   }
-  return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, pdl, 2, a, b, b3, s, ws, timeout_ns,
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, pdl, 2, a, b, b3, y, s, ws, timeout_ns,
                        stall ? 1 : 0);
 }
 
@@ -368,17 +418,18 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 
 cudaError_t launch_gemm_tc_pair(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
                                 int64_t timeout_ns, bool test_stall, bool pdl, cudaStream_t st) {
-  CUtensorMap mA, mB, mB3;
+  CUtensorMap mA, mB, mB3, mY;
   cudaError_t e;
   if (mode == 1) {
     if ((e = make_tmap_bf16(&mA, ws.xp, (uint64_t)s.N, (uint64_t)s.d, kRowsPerCta)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB, w.w1, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB3, w.w3, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
-    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, s, ws, num_sms, timeout_ns, test_stall, pdl, st);
+    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, mA, s, ws, num_sms, timeout_ns, test_stall, pdl, st);
   }
   if ((e = make_tmap_bf16(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kRowsPerCta)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN / 2)) != cudaSuccess) return e;
-  return launch_pair<2, kPairAccBufs>(mA, mB, mB, s, ws, num_sms, timeout_ns, false, pdl, st);
+  if ((e = make_tmap_bf16(&mY, ws.yp, (uint64_t)s.N, (uint64_t)s.d, 32)) != cudaSuccess) return e;
+  return launch_pair<2, kPairAccBufs>(mA, mB, mB, mY, s, ws, num_sms, timeout_ns, false, pdl, st);
 }
 
 }  // namespace moe

@@ -44,10 +44,12 @@ struct Ws {
   int32_t* counts;      // [E]
   int32_t* offsets;     // [E+1]
   int32_t* blk_base;    // [nblk, E] first row of (block, expert) in dispatch order
-  int32_t* grp_expert;  // [max_groups] expert of scheduling group g
-  int32_t* grp_mtile0;  // [max_groups] first m-tile (within the expert) of group g
-  int32_t* grp_mpre;    // [max_groups+1] prefix count of m-tiles over groups
-  int32_t* grp_ppre;    // [max_groups+1] prefix count of m-tile pairs (ceil(m-tiles / 2)) over groups
+  // Tile descriptors: entry q describes the scheduling group that owns m-tile q (mt_desc) or
+  // m-tile pair q (pr_desc), so that a tile id decodes with one load:
+  //   x = expert | (m-tiles, resp. pairs, of the group) << 20, y = the group's first m-tile
+  //   (pair) index, z = the group's first row, w = one past the expert's last row.
+  int4* mt_desc;        // [max_groups * kGroupM]
+  int4* pr_desc;        // [max_groups * kGroupM / 2]
   int32_t* perm_src;    // [N]
   int32_t* perm_slot;   // [N]
   float* gate_perm;     // [N]
@@ -55,7 +57,7 @@ struct Ws {
   float* logits;        // [T, E] or null
   void* xp;             // [N, d]
   void* h;              // [N, F]
-  void* yslot;          // [N, d]
+  void* yp;             // [N, d] gate * expert output of routed row p (expert order)
   // training (forward keeps, backward uses)
   void* a1;             // [N, F] bf16: W1_e . x of each routed row
   void* a3;             // [N, F] bf16: W3_e . x
@@ -75,8 +77,8 @@ struct Ws {
 // Fixed layout of one workspace: byte offsets of each region.
 struct WsLayout {
   size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
-      grp_expert, grp_mtile0, grp_mpre, grp_ppre, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
-      yslot, a1, a3, probs, dyp, dop, dab, dgp, dxslot, dlogit, dl_hi, dl_lo, dwr_part, dwr_part_b, total;
+      mt_desc, pr_desc, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
+      yp, a1, a3, probs, dyp, dop, dab, dgp, dxslot, dlogit, dl_hi, dl_lo, dwr_part, dwr_part_b, total;
 };
 
 // Columns of the bf16 dlogit terms: E rounded up to 64 (a whole 128-byte TMA box).

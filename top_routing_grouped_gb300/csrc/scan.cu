@@ -108,17 +108,17 @@ __global__ void __launch_bounds__(kScanBlock) scan_kernel(Shape s, Ws ws) {
     ws.counts[e] = cnt;
     ws.offsets[e] = off;
     for (int g = 0; g < ng; ++g) {
-      ws.grp_expert[gstart + g] = e;
-      ws.grp_mtile0[gstart + g] = g * kGroupM;
-      ws.grp_mpre[gstart + g] = mstart + g * kGroupM;
-      ws.grp_ppre[gstart + g] = pstart + g * (kGroupM / 2);
+      const int gm = g + 1 < ng ? kGroupM : last_gm;  // m-tiles of this group
+      const int gp = (gm + 1) / 2;                      // and pairs
+      const int m0 = mstart + g * kGroupM, p0 = pstart + g * (kGroupM / 2);
+      const int row0 = off + g * kGroupM * kTileM;
+      for (int i = 0; i < gm; ++i) ws.mt_desc[m0 + i] = make_int4(e | (gm << 20), m0, row0, off + cnt);
+      for (int i = 0; i < gp; ++i) ws.pr_desc[p0 + i] = make_int4(e | (gp << 20), p0, row0, off + cnt);
     }
     buf[e] = off;  // the experts' offsets, for the per-block bases below
   }
   if (e == 0) {
     ws.offsets[E] = n_routed;
-    ws.grp_mpre[n_groups] = n_mtiles;
-    ws.grp_ppre[n_groups] = n_pairs;
     ws.hdr[kHdrNumGroups] = (uint32_t)n_groups;
     ws.hdr[kHdrNumMTiles] = (uint32_t)n_mtiles;
     ws.hdr[kHdrNumPairs] = (uint32_t)n_pairs;

@@ -35,7 +35,7 @@ class MoeConfig(ctypes.Structure):
 class MoeViews(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "status", "aux", "topk_idx", "topk_gate", "expert_counts", "expert_offsets", "perm_src",
-        "perm_slot", "gate_perm", "slot_pos", "logits", "xp", "h", "yslot")]
+        "perm_slot", "gate_perm", "slot_pos", "logits", "xp", "h", "yp")]
 
 
 _P = ctypes.c_void_p
@@ -225,4 +225,4 @@ class MoEPlan:
             perm_src=view(v.perm_src, i32, (N,)), perm_slot=view(v.perm_slot, i32, (N,)),
             gate_perm=view(v.gate_perm, f32, (N,)), slot_pos=view(v.slot_pos, i32, (N,)),
             logits=view(v.logits, f32, (self.T, self.E)), xp=view(v.xp, act, (N, self.d)),
-            h=view(v.h, act, (N, self.F)), yslot=view(v.yslot, act, (N, self.d)))
+            h=view(v.h, act, (N, self.F)), yp=view(v.yp, act, (N, self.d)))

@@ -12,12 +12,12 @@
 // Both CTAs' loads signal the leader's "full" barrier; the leader's commits free the stage in
 // both CTAs (multicast arrive) and hand each CTA its 128 accumulator rows in its own TMEM.
 // The epilogue runs per CTA; its warps release the accumulator to the leader with a
-// cluster-scope arrive.  Mode 1 stores its H rows directly.  Mode 2 writes Yp in the same
-// expert-contiguous row order as its A operand, so each warp's 32 rows x 64 columns form one
-// tile of Yp: the warp stages it in shared memory (128-byte swizzle, double-buffered) and one
-// lane hands it to the TMA engine as a tiled store.  Only a warp block that crosses the end of
-// the expert's rows stores its valid rows directly (a tiled store would overwrite the next
-// expert's first rows).
+// cluster-scope arrive.  Both outputs (H, Yp) are in the expert-contiguous row order of the A
+// operand, so each warp's 32 rows x 64 columns form one tile of the output: the warp stages it
+// in shared memory (128-byte swizzle, double-buffered) and one lane hands it to the TMA engine
+// as a tiled store.  Only a warp block that crosses the end of the expert's rows stores its
+// valid rows directly (a tiled store would overwrite the next expert's first rows).  In
+// training mode W1.x and W3.x are also kept, stored directly.
 //
 // Waits are bounded (MOE_ERR_TIMEOUT, no trap); an abort raises the flag in both CTAs; the
 // pair meets at cluster barriers before TMEM is released.
@@ -31,7 +31,7 @@ namespace moe {
 namespace {
 
 constexpr int kBK = 64;
-constexpr int kStages = 6;  // ring depth of mode 1; mode 2 gives one stage to its store staging
+constexpr int kStages = 6;
 constexpr int kRowsPerCta = 128;
 constexpr int kMmaM = 256;  // both CTAs
 constexpr int kMmaN = 256;
@@ -55,19 +55,13 @@ struct Ctl2 {
   int abort;
 };
 
-// mode 2's store staging: per epilogue warp two blocks of 32 rows x 64 bf16 columns (128-byte
+// the epilogue's store staging: per warp two blocks of 32 rows x 64 bf16 columns (128-byte
 // rows, 16-byte chunk j of row r at j ^ (r % 8): the TMA 128-byte swizzle), 1024-byte aligned
 constexpr int kStgBlockBytes = 32 * 128;
 constexpr int kStgBytes = kEpiWarps * 2 * kStgBlockBytes;
 
-template <int kMode>
-constexpr int ring_stages() { return kMode == 1 ? kStages : kStages - 1; }
-
-template <int kMode>
-constexpr size_t smem_bytes() {
-  return 1024 + (size_t)ring_stages<kMode>() * kStageBytes + (kMode == 2 ? kStgBytes : 0) + sizeof(Ctl2);
-}
-static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448, "shared memory per CTA");
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kStgBytes + sizeof(Ctl2);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -93,6 +87,32 @@ __device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bu
 // all of this thread's bulk groups complete (their global writes performed)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Store 64 bf16 columns of this warp's 32 rows (pk: this lane's row).  When all 32 rows
+// belong to the tile's expert (vw >= 32) the warp stages them in its next staging block and
+// lane 0 issues one tiled store of the block at (x, y); otherwise each lane whose row is valid
+// (lane < vw) writes its 128 bytes to dst directly, so that no row of the next expert is
+// touched.  vw is the same for the whole warp.
+__device__ __forceinline__ void store_rows64(const uint32_t (&pk)[32], int vw, int lane, uint32_t stg,
+                                             int& stg_buf, const CUtensorMap* map, int x, int y, void* dst) {
+  if (vw >= 32) {
+    const uint32_t blk = stg + (uint32_t)(stg_buf * kStgBlockBytes);
+    if (lane == 0) bulk_wait_read_le1();  // the store issued from this block two blocks ago has read it
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(blk + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) * 16)), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                   pk[4 * j + 3]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA engine
+    __syncwarp();
+    if (lane == 0) tma_store_2d(map, x, y, blk);
+    stg_buf ^= 1;
+  } else if (lane < vw) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  }
+}
+
 __device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
   ctl->abort = 1;
   ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&ctl->abort), rank ^ 1u), 1u);
@@ -105,9 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     Ws ws, int64_t timeout_ns, int stall) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kRing = ring_stages<kMode>();
-  uint8_t* stg_base = stages + kRing * kStageBytes;  // mode 2's store staging
-  Ctl2* ctl = reinterpret_cast<Ctl2*>(stg_base + (kMode == 2 ? kStgBytes : 0));
+  uint8_t* stg_base = stages + kStages * kStageBytes;  // the epilogue's store staging
+  Ctl2* ctl = reinterpret_cast<Ctl2*>(stg_base + kStgBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -122,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kblocks = K / kBK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       ptx::mbar_init(ptx::smem_u32(&ctl->full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&ctl->empty[i]), 1);
     }
@@ -139,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
     if (kMode == 1) ptx::tma_prefetch_desc(&tmB3);
-    if (kMode == 2) ptx::tma_prefetch_desc(&tmY);
+    ptx::tma_prefetch_desc(&tmY);
   }
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive or load
   if (warp == 2) {
@@ -185,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_load_2d_pair(sa + kABytes, bmap, kb * kBK, brow, bar);
           }
           first = false;
-          if (++stage == kRing) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -224,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_bf16_pair(d_tmem, ptx::desc_kmajor_sw128(sa + ks * kMmaK * 2),
                                ptx::desc_kmajor_sw128(sb + ks * kMmaK * 2), idesc, (kb | ks) != 0 ? 1u : 0u);
           ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
-          if (++stage == kRing) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -247,9 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t stg = ptx::smem_u32(stg_base) + (uint32_t)(q * 2 * kStgBlockBytes);
-    int stg_buf = 0;  // the staging block this lane's next copy uses
-    (void)stg;
-    (void)stg_buf;
+    int stg_buf = 0;  // the staging block of this warp's next tiled store
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -263,85 +280,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = r < ti.rows;
       const int64_t p = (int64_t)ti.row0 + r;
       const int n0 = ti.n_idx * bn;
+      // rows of this warp's 32-row block that belong to the tile's expert: all 32 -> one tiled
+      // store per 64 columns; fewer -> each valid lane stores its own row piece
+      const int vw = ti.rows - q * 32;
       if (kMode == 1) {
         __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(ws.h) + p * s.F + n0;
 #pragma unroll 1
-        for (int c = 0; c < kMmaN / 2; c += 32) {
-          uint32_t a[32], g[32];
-          ptx::tmem_ld_32cols(t_row + c, a);
-          ptx::tmem_ld_32cols(t_row + kMmaN / 2 + c, g);
-          ptx::tmem_ld_wait();
-          if (valid && n0 + c < s.F) {
-            uint4* dst = reinterpret_cast<uint4*>(hrow + c);
+        for (int c = 0; c < kMmaN / 2; c += 64) {
+          if (vw <= 0 || n0 + c >= s.F) break;  // warp-uniform
+          uint32_t pk[32];  // the row's 64 H values
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t a[32], g[32];
+            ptx::tmem_ld_32cols(t_row + c + 32 * hh, a);
+            ptx::tmem_ld_32cols(t_row + kMmaN / 2 + c + 32 * hh, g);
+            ptx::tmem_ld_wait();
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int i = v * 8 + u * 2;
-                ow[u] = pack_bf16x2(silu(__uint_as_float(a[i])) * __uint_as_float(g[i]),
-                                    silu(__uint_as_float(a[i + 1])) * __uint_as_float(g[i + 1]));
-              }
-              dst[v] = o;
-            }
-            if (s.training) {  // keep W1.x and W3.x of the row for the backward
-              uint4* da1 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.a1) + p * s.F + n0 + c);
-              uint4* da3 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.a3) + p * s.F + n0 + c);
+            for (int i = 0; i < 16; ++i)
+              pk[16 * hh + i] = pack_bf16x2(silu(__uint_as_float(a[2 * i])) * __uint_as_float(g[2 * i]),
+                                            silu(__uint_as_float(a[2 * i + 1])) * __uint_as_float(g[2 * i + 1]));
+            if (s.training && valid) {  // keep W1.x and W3.x of the row for the backward
+              const int64_t o = p * s.F + n0 + c + 32 * hh;
+              uint4* da1 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.a1) + o);
+              uint4* da3 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.a3) + o);
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
-                uint4 o1, o3;
-                uint32_t* w1p = reinterpret_cast<uint32_t*>(&o1);
-                uint32_t* w3p = reinterpret_cast<uint32_t*>(&o3);
+                uint32_t w1[4], w3[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                   const int i = v * 8 + u * 2;
-                  w1p[u] = pack_bf16x2(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
-                  w3p[u] = pack_bf16x2(__uint_as_float(g[i]), __uint_as_float(g[i + 1]));
+                  w1[u] = pack_bf16x2(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+                  w3[u] = pack_bf16x2(__uint_as_float(g[i]), __uint_as_float(g[i + 1]));
                 }
-                da1[v] = o1;
-                da3[v] = o3;
+                da1[v] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                da3[v] = make_uint4(w3[0], w3[1], w3[2], w3[3]);
               }
             }
           }
+          store_rows64(pk, vw, lane, stg, stg_buf, &tmY, n0 + c, ti.row0 + q * 32, hrow + c);
         }
       } else {
         const float gate = valid ? ws.gate_perm[p] : 0.f;
-        // rows of this warp's 32-row block that belong to the tile's expert: all 32 -> one
-        // tiled store per 64 columns; fewer -> each valid lane stores its own row piece
-        const int vw = ti.rows - q * 32;
         __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(ws.yp) + p * s.d + n0;
 #pragma unroll 1
         for (int c = 0; c < kMmaN; c += 64) {
+          if (vw <= 0 || n0 + c >= s.d) break;  // warp-uniform
           uint32_t a[32], b[32];
           ptx::tmem_ld_32cols(t_row + c, a);
           ptx::tmem_ld_32cols(t_row + c + 32, b);
           ptx::tmem_ld_wait();
-          if (vw > 0 && n0 + c < s.d) {  // warp-uniform
-            uint32_t pk[32];  // the row's 64 bf16 values
+          uint32_t pk[32];  // the row's 64 output values
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              pk[i] = pack_bf16x2(gate * __uint_as_float(a[2 * i]), gate * __uint_as_float(a[2 * i + 1]));
-              pk[16 + i] = pack_bf16x2(gate * __uint_as_float(b[2 * i]), gate * __uint_as_float(b[2 * i + 1]));
-            }
-            if (vw >= 32) {
-              const uint32_t blk = stg + (uint32_t)(stg_buf * kStgBlockBytes);
-              if (lane == 0) bulk_wait_read_le1();  // the store issued from this block two chunks ago has read it
-              __syncwarp();
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                st_shared_v4(blk + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) * 16)), pk[4 * j], pk[4 * j + 1],
-                             pk[4 * j + 2], pk[4 * j + 3]);
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA engine
-              __syncwarp();
-              if (lane == 0) tma_store_2d(&tmY, n0 + c, ti.row0 + q * 32, blk);
-              stg_buf ^= 1;
-            } else if (lane < vw) {
-              uint4* dst = reinterpret_cast<uint4*>(yrow + c);
-#pragma unroll
-              for (int v = 0; v < 8; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
+          for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16x2(gate * __uint_as_float(a[2 * i]), gate * __uint_as_float(a[2 * i + 1]));
+            pk[16 + i] = pack_bf16x2(gate * __uint_as_float(b[2 * i]), gate * __uint_as_float(b[2 * i + 1]));
           }
+          store_rows64(pk, vw, lane, stg, stg_buf, &tmY, n0 + c, ti.row0 + q * 32, yrow + c);
         }
       }
       ptx::tc_fence_before();
@@ -352,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    if (kMode == 2) bulk_wait_all();  // the tiled stores this lane issued have been written
+    bulk_wait_all();  // the tiled stores this lane issued have been written
     if (!ok && lane == 0) {
       record_error(ws, MOE_ERR_TIMEOUT, 0x570u + kMode);
       raise_abort(ctl, rank);
@@ -389,7 +383,6 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtens
                         const Shape& s, const Ws& ws,
                         int num_sms, int64_t timeout_ns, bool stall, bool pdl, cudaStream_t st) {
   auto kern = gemm_tc2_kernel<kMode, kAccBufs>;
-  constexpr size_t kSmemBytes = smem_bytes<kMode>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   // as many pairs as can be resident at once (persistent loop over pair tiles)
@@ -424,7 +417,8 @@ cudaError_t launch_gemm_tc_pair(int mode, const Shape& s, const Ws& ws, const We
     if ((e = make_tmap_bf16(&mA, ws.xp, (uint64_t)s.N, (uint64_t)s.d, kRowsPerCta)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB, w.w1, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mB3, w.w3, (uint64_t)s.E * s.F, (uint64_t)s.d, kMmaN / 2)) != cudaSuccess) return e;
-    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, mA, s, ws, num_sms, timeout_ns, test_stall, pdl, st);
+    if ((e = make_tmap_bf16(&mY, ws.h, (uint64_t)s.N, (uint64_t)s.F, 32)) != cudaSuccess) return e;
+    return launch_pair<1, kPairAccBufs>(mA, mB, mB3, mY, s, ws, num_sms, timeout_ns, test_stall, pdl, st);
   }
   if ((e = make_tmap_bf16(&mA, ws.h, (uint64_t)s.N, (uint64_t)s.F, kRowsPerCta)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16(&mB, w.w2, (uint64_t)s.E * s.d, (uint64_t)s.F, kMmaN / 2)) != cudaSuccess) return e;

@@ -29,7 +29,7 @@ struct Shape {
   int training;   // the forward keeps what the backward needs (pre-activations, softmax)
   int act_bf16;   // x and weights are bf16 (else fp32)
   int out_bf16;   // y is bf16 (else fp32)
-  int max_groups; // capacity of the group table
+  int max_groups; // bound on the scheduling groups (sizes the tile descriptors)
 };
 
 // Device pointers into one workspace.

@@ -434,6 +434,9 @@ def main():
     st = plan.device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
+    # rows the pair GEMMs multiply: each expert's rows rounded up to whole 256-row pair tiles
+    counts = plan.views(ws)["expert_counts"].cpu().tolist()
+    pair_rows = 256 * sum((c + 255) // 256 for c in counts)
 
     K = args.steps
     # timed region 1: whole forwards (one event pair per step; the kernels of a forward are
@@ -593,7 +596,11 @@ def main():
             "roofline": {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": g1_tflops, "peak": pk["bf16"],
                          "unit": "TFLOP/s", "frac": g1_tflops / pk["bf16"], "traffic": traffic,
                          "peak_source": f"{pk['src']} bf16 burst", "frac_of_sustained": g1_tflops / pk["bf16_sust"],
-                         "algorithmic": f"4*N*d*F = {g1_flops} FLOP per launch (N = T*k = {shape.N} rows)"},
+                         "algorithmic": f"4*N*d*F = {g1_flops} FLOP per launch (N = T*k = {shape.N} rows)",
+                         "executed": {"rows": pair_rows, "tflops": g1_tflops * pair_rows / shape.N,
+                                      "frac_of_sustained": g1_tflops * pair_rows / shape.N / pk["bf16_sust"],
+                                      "note": "the tensor cores also multiply the padding of each expert's last "
+                                              "256-row pair tile; achieved counts the N routed rows only"}},
             "graph": {"ms_per_step": graph_max_ms / K, "tokens_per_s": throughput(shape.T, K, world, graph_max_ms),
                       "from": "one forward captured into a CUDA graph, K replays (timed region 4)"},
             "e2e": e2e,

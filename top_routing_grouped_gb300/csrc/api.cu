@@ -110,6 +110,8 @@ WsLayout ws_layout(const Shape& s) {
     L.dyp = take(N * (size_t)s.d * 2);
     L.dop = take(N * (size_t)s.d * 2);
     L.dab = take(N * 2 * (size_t)s.F * 2);
+    L.dab_tail = take(E * 64 * 2 * (size_t)s.F * 2);
+    L.dop_tail = take(E * 64 * (size_t)s.d * 2);
     L.dgp = take(N * nt * 4);
     L.dxslot = take(N * (size_t)s.d * 2);
     L.dlogit = take((size_t)s.T * E * 4);
@@ -153,6 +155,8 @@ Ws ws_bind(const Shape& s, void* base) {
     w.dyp = b + L.dyp;
     w.dop = b + L.dop;
     w.dab = b + L.dab;
+    w.dab_tail = b + L.dab_tail;
+    w.dop_tail = b + L.dop_tail;
     w.dgp = reinterpret_cast<float*>(b + L.dgp);
     w.dxslot = b + L.dxslot;
     w.dlogit = reinterpret_cast<float*>(b + L.dlogit);

@@ -46,7 +46,9 @@ __device__ __forceinline__ uint4 pack8(const float* f, float scale) {
   return o;
 }
 
-// One warp per token: read dy[t] once, write its k dispatched rows (plain and gate-scaled).
+// One warp per token: read dy[t] once, write its k dispatched rows (plain and gate-scaled; a
+// gate-scaled row in its expert's last, partial 64-row block also to dop_tail).  Then the
+// warps zero the rows of dop_tail and dab_tail past each expert's end.
 __global__ void __launch_bounds__(kGatherWarps * 32) gather_dy_kernel(Shape s, Ws ws, const void* dy) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
@@ -55,15 +57,17 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_dy_kernel(Shape s, W
   pdl_wait();
   pdl_launch_dependents();
   for (int64_t t = warp; t < s.T; t += nwarps) {
-    int64_t my_p = -1;
+    int64_t my_p = -1, my_tr = -1;  // row in dyp / dop, row in dop_tail (or -1)
     float my_g = 0.f;
     if (lane < s.k) {
       my_p = ws.slot_pos[t * s.k + lane];
-      if (my_p < 0 || my_p >= s.N) {
+      const int e = ws.topk_idx[t * s.k + lane];
+      if (my_p < 0 || my_p >= s.N || e < 0 || e >= s.E) {
         record_error(ws, MOE_ERR_INTERNAL, 0x900u);
         my_p = -1;
       } else {
         my_g = ws.gate_perm[my_p];
+        my_tr = tail_row(e, my_p, ws.offsets[e], ws.counts[e]);
       }
     }
     for (int v = lane; v < v8; v += 32) {
@@ -71,12 +75,25 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_dy_kernel(Shape s, W
       load8(dy, s.out_bf16, t * v8 + v, f);
       for (int j = 0; j < s.k; ++j) {
         const int64_t p = __shfl_sync(0xffffffffu, my_p, j);
+        const int64_t tr = __shfl_sync(0xffffffffu, my_tr, j);
         const float g = __shfl_sync(0xffffffffu, my_g, j);
         if (p < 0) continue;
         reinterpret_cast<uint4*>(ws.dyp)[p * v8 + v] = pack8(f, 1.f);
-        reinterpret_cast<uint4*>(ws.dop)[p * v8 + v] = pack8(f, g);
+        const uint4 o = pack8(f, g);
+        reinterpret_cast<uint4*>(ws.dop)[p * v8 + v] = o;
+        if (tr >= 0) reinterpret_cast<uint4*>(ws.dop_tail)[tr * v8 + v] = o;
       }
     }
+  }
+  // rows r of expert e's tail block at or past its count there are zero
+  const int f8 = (2 * s.F) / 8;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t u = warp; u < (int64_t)s.E * 64; u += nwarps) {
+    const int e = (int)(u / 64), r = (int)(u % 64);
+    const int rem = ws.counts[e] % 64;
+    if (rem == 0 || r < rem) continue;  // no tail block, or a routed row
+    for (int v = lane; v < v8; v += 32) reinterpret_cast<uint4*>(ws.dop_tail)[u * v8 + v] = z;
+    for (int v = lane; v < f8; v += 32) reinterpret_cast<uint4*>(ws.dab_tail)[u * f8 + v] = z;
   }
 }
 

@@ -11,8 +11,9 @@
 //   kDW13 [dW1_e; dW3_e][m, c] = sum_{p in e} [da|db][p, m] Xp[p, c]   (both operands MN-major)
 //   kDW2  dW2_e[c, f]          = sum_{p in e} g dy[t, c] h[p, f]       (both operands MN-major)
 // kDH and kDX are grouped over M (the expert's rows, the forward's tile table); kDW13 and
-// kDW2 over K (the expert's rows are the reduction: its last 64-row K block is cut at the
-// expert's end by zeroing the A rows past it in shared memory before the MMA reads them).
+// kDW2 over K (the expert's rows are the reduction).  An expert's last, partial 64-row K
+// block of A comes from dab_tail / dop_tail (the same rows, zero past the expert's end), so
+// no block is masked; B (Xp, h) runs on into the next expert's rows, which the zeros cancel.
 //
 // MN-major operand tiles: TMA boxes of 64 (MN, contiguous) x 64 (K rows) with 128-byte
 // swizzling, side by side 8 KB apart; the descriptor's leading offset is that 8 KB step
@@ -98,7 +99,7 @@ struct BTile {
   int n_idx;
   int k_row0;       // K-grouped: first routed row of the expert (the K range)
   int kblocks;
-  int k_tail;       // valid rows of the last K block (1..64), K-grouped only
+  int a_tail;       // K-grouped: row of the expert's tail block in dab_tail / dop_tail, or -1
 };
 
 struct BwdArgs {
@@ -128,8 +129,8 @@ __device__ __forceinline__ BTile decode(const BwdArgs& a, int tile, int n_tiles,
     b.rows = ti.rows;
     b.n_idx = ti.n_idx;
     b.kblocks = K / kBK;
-    b.k_tail = kBK;
     b.k_row0 = 0;
+    b.a_tail = -1;
   } else {
     int M, N, K;
     kind_dims<kKind>(a.s, M, N, K);
@@ -143,7 +144,7 @@ __device__ __forceinline__ BTile decode(const BwdArgs& a, int tile, int n_tiles,
     const int cnt = __ldg(&a.ws.counts[b.e]);
     b.k_row0 = __ldg(&a.ws.offsets[b.e]);
     b.kblocks = (cnt + kBK - 1) / kBK;
-    b.k_tail = cnt - (b.kblocks - 1) * kBK;
+    b.a_tail = cnt % kBK != 0 ? b.e * kBK : -1;
   }
   return b;
 }
@@ -214,9 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!a_mn(kKind)) {
             ptx::tma_load_2d(sa, &tmA, kb * kBK, bt.row0, bar);  // [rows, K]: one 128-row box
           } else {
-            const int krow = bt.k_row0 + kb * kBK;
-            ptx::tma_load_2d(sa, &tmA, bt.row0, krow, bar);
-            ptx::tma_load_2d(sa + kBoxBytes, &tmA, bt.row0 + 64, krow, bar);
+            // the expert's last, partial block from the zero-padded tail copy (tmB2 slot)
+            const bool tail = kb == bt.kblocks - 1 && bt.a_tail >= 0;
+            const CUtensorMap* am = tail ? &tmB2 : &tmA;
+            const int krow = tail ? bt.a_tail : bt.k_row0 + kb * kBK;
+            ptx::tma_load_2d(sa, am, bt.row0, krow, bar);
+            ptx::tma_load_2d(sa + kBoxBytes, am, bt.row0 + 64, krow, bar);
           }
           // B: four MN-major boxes of 64 columns
           const CUtensorMap* bm = &tmB;
@@ -247,8 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer (whole warp:
-    // the lanes zero the rows past an expert's end in its last K block)
+    // -------------------------------------------------------------- MMA issuer
     const uint32_t idesc = ptx::idesc_bf16_f32(kTM, kTN) | (a_mn(kKind) ? (1u << 15) : 0u) | (1u << 16);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -265,18 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         uint8_t* st_base = stages + (size_t)stage * kStageBytes;
-        if (k_grouped(kKind) && kb == bt.kblocks - 1 && bt.k_tail < kBK) {
-          // A is MN-major: K row r of box j is the 128-byte line j*8KB + r*128; zero rows
-          // k_tail..63 of both boxes (whole lines, so the swizzle does not matter)
-          const int lines = kBK - bt.k_tail;
-          for (int i = lane; i < 2 * lines * 8; i += 32) {
-            const int box = i / (lines * 8), rem = i % (lines * 8);
-            const int line = bt.k_tail + rem / 8, chunk = rem % 8;
-            *reinterpret_cast<uint4*>(st_base + box * kBoxBytes + line * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-        }
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t sa = ptx::smem_u32(st_base);
@@ -336,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int F = s.F;
         const float g = valid ? ws.gate_perm[p] : 0.f;
         __nv_bfloat16* darow = reinterpret_cast<__nv_bfloat16*>(ws.dab) + p * 2 * F + n0;
+        const int64_t trow = valid ? tail_row(bt.e, p, __ldg(&ws.offsets[bt.e]), __ldg(&ws.counts[bt.e])) : -1;
+        __nv_bfloat16* dtrow = reinterpret_cast<__nv_bfloat16*>(ws.dab_tail) + (trow >= 0 ? trow : 0) * 2 * F + n0;
         float dg = 0.f;
 #pragma unroll
         for (int i = 0; i < (kTN / 2) / 16; ++i) {
@@ -373,6 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 *reinterpret_cast<uint4*>(darow + c + 8 * u) = oa;
                 *reinterpret_cast<uint4*>(darow + F + c + 8 * u) = ob;
+                if (trow >= 0) {
+                  *reinterpret_cast<uint4*>(dtrow + c + 8 * u) = oa;
+                  *reinterpret_cast<uint4*>(dtrow + F + c + 8 * u) = ob;
+                }
               }
             }
           }
@@ -503,14 +500,16 @@ cudaError_t launch_gemm_bwd(int kind, const Shape& s, const Ws& ws, const Weight
     case kBwdDW13:
       if ((e = make_tmap_bf16(&ma, ws.dab, N, 2 * F, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb, ws.xp, N, d, 64)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb2, ws.dab_tail, E * 64, 2 * F, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_f32_rows128(&mo1, dw_a, E * F, d, 32)) != cudaSuccess) return e;
       if ((e = make_tmap_f32_rows128(&mo2, dw_b, E * F, d, 32)) != cudaSuccess) return e;
-      return launch_kind<kBwdDW13>(ma, mb, mb, mo1, mo2, args, num_sms, timeout_ns, pdl, st);
+      return launch_kind<kBwdDW13>(ma, mb, mb2, mo1, mo2, args, num_sms, timeout_ns, pdl, st);
     case kBwdDW2:
       if ((e = make_tmap_bf16(&ma, ws.dop, N, d, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_bf16(&mb, ws.h, N, F, 64)) != cudaSuccess) return e;
+      if ((e = make_tmap_bf16(&mb2, ws.dop_tail, E * 64, d, 64)) != cudaSuccess) return e;
       if ((e = make_tmap_f32_rows128(&mo1, dw_a, E * d, F, 32)) != cudaSuccess) return e;
-      return launch_kind<kBwdDW2>(ma, mb, mb, mo1, mo1, args, num_sms, timeout_ns, pdl, st);
+      return launch_kind<kBwdDW2>(ma, mb, mb2, mo1, mo1, args, num_sms, timeout_ns, pdl, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -13,7 +13,8 @@
 // free the stage in both CTAs and hand each CTA its 128 accumulator rows.  The dH epilogue
 // turns each 32 x 32 block of dH' around in shared memory so that its loads of h, a, b and
 // its stores of [da | db] move whole 64-byte row segments per four lanes; the dX epilogue
-// is the one-SM kernel's (gemm_bwd.cu).
+// is the one-SM kernel's (gemm_bwd.cu).  A [da | db] row in its expert's last, partial 64-row
+// block is also written to dab_tail, which the weight-gradient GEMMs read for that block.
 //
 // Waits are bounded (MOE_ERR_TIMEOUT, no trap); an abort raises the flag in both CTAs; the
 // pair meets at cluster barriers before TMEM is released.
@@ -270,6 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kKind == kBwdDH) {
         const int F = s.F;
         const uint32_t xb = ptx::smem_u32(xpose + (warp - kEpiWarp0) * kXposeBytes);
+        int64_t trow[4];  // rows of dab_tail (or -1)
+        {
+          const int off_e = __ldg(&ws.offsets[ti.e]), cnt_e = __ldg(&ws.counts[ti.e]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) trow[i] = rv[i] ? tail_row(ti.e, prow[i], off_e, cnt_e) : -1;
+        }
         float g[4], dgacc[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -321,6 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               __nv_bfloat16* dr = reinterpret_cast<__nv_bfloat16*>(ws.dab) + prow[i] * 2 * F + n0 + c + cg;
               *reinterpret_cast<uint4*>(dr) = oa;
               *reinterpret_cast<uint4*>(dr + F) = ob;
+              if (trow[i] >= 0) {
+                __nv_bfloat16* tr = reinterpret_cast<__nv_bfloat16*>(ws.dab_tail) + trow[i] * 2 * F + n0 + c + cg;
+                *reinterpret_cast<uint4*>(tr) = oa;
+                *reinterpret_cast<uint4*>(tr + F) = ob;
+              }
             }
           }
           __syncwarp();  // the block is read before the next chunk overwrites it

@@ -9,11 +9,11 @@
 // computes a 256 (weight rows) x 256 (columns) tile: each CTA loads its own 128 weight rows of
 // A and 128 of the 256 B columns for the same K rows.
 //
-// The K range is the expert's rows, so its last 64-row block runs past the expert's end into
-// the next expert's rows; those A rows are zeroed in shared memory before the MMA reads them,
-// in both CTAs.  The leader zeroes its own after its bytes land; the peer loads that block
-// with its own barrier (not the leader's), zeroes, and then arrives on the leader's per-stage
-// "zeroed" barrier, which the leader waits on before that block's MMAs.
+// The K range is the expert's rows, so its last 64-row block runs past the expert's end.  For
+// that block A comes from dab_tail / dop_tail, which repeat the expert's rows of that block and
+// are zero past its end; B (Xp, h) runs on into the next expert's rows (or TMA's zero fill past
+// the last row), which the zeros cancel.  Every block is an ordinary pair load: no block is
+// masked in shared memory and the two CTAs need no extra handshake.
 //
 // The fp32 gradient leaves through 32 x 32 swizzled shared-memory blocks and TMA stores.
 // Waits are bounded (MOE_ERR_TIMEOUT, no trap); an abort raises the flag in both CTAs; the
@@ -46,10 +46,8 @@ constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, one per 128-column h
 constexpr int kOutBlockBytes = 32 * 128;
 
 struct Ctl3 {
-  uint64_t full[kStages];    // leader's: the stage's bytes (both CTAs', or its own in a tail block)
+  uint64_t full[kStages];    // leader's: the stage's bytes (both CTAs')
   uint64_t empty[kStages];   // each CTA: stage free again (leader's multicast commit)
-  uint64_t pfull[kStages];   // peer's: its own bytes of a tail block
-  uint64_t zready[kStages];  // leader's: the peer has zeroed its rows of a tail block
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -63,7 +61,8 @@ constexpr size_t kSmemBytes =
 
 struct KTile {
   int e, n_idx, row0, rows;  // row0/rows: this CTA's weight rows (rows <= 0: none)
-  int k_row0, kblocks, k_tail;
+  int k_row0, kblocks;
+  int a_tail;  // row of the expert's last, partial block in dab_tail / dop_tail, or -1
 };
 
 template <int kKind>
@@ -79,7 +78,7 @@ __device__ __forceinline__ KTile decode_k(const Shape& s, const Ws& ws, int tile
   const int cnt = __ldg(&ws.counts[t.e]);
   t.k_row0 = __ldg(&ws.offsets[t.e]);
   t.kblocks = (cnt + kBK - 1) / kBK;
-  t.k_tail = cnt - (t.kblocks - 1) * kBK;
+  t.a_tail = cnt % kBK != 0 ? t.e * kBK : -1;
   return t;
 }
 
@@ -88,22 +87,10 @@ __device__ __forceinline__ void raise_abort(Ctl3* ctl, uint32_t rank) {
   ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&ctl->abort), rank ^ 1u), 1u);
 }
 
-// Zero K rows k_tail..63 of the two A boxes of a stage (whole 128-byte lines, so the swizzle
-// does not matter), then make the zeros visible to the tensor cores; a whole warp calls it.
-__device__ __forceinline__ void zero_a_tail(uint8_t* st_base, int k_tail, int lane) {
-  const int lines = kBK - k_tail;
-  for (int i = lane; i < 2 * lines * 8; i += 32) {
-    const int box = i / (lines * 8), rem = i % (lines * 8);
-    const int line = k_tail + rem / 8, chunk = rem % 8;
-    *reinterpret_cast<uint4*>(st_base + box * kBoxBytes + line * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncwarp();
-}
-
 template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_dw_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_dw_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAT,
+                        const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2, Shape s,
                         Ws ws, int64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -127,8 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       ptx::mbar_init(ptx::smem_u32(&ctl->full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&ctl->empty[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&ctl->pfull[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&ctl->zready[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&ctl->tfull[i]), 1);
@@ -141,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmAT);
     ptx::tma_prefetch_desc(&tmB);
   }
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive or load
@@ -177,28 +163,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const bool tail = kb == kt.kblocks - 1 && kt.k_tail < kBK;
-          const int krow = kt.k_row0 + kb * kBK;
+          const int krow = kt.k_row0 + kb * kBK;  // B: Xp / h rows
+          const bool tail = kb == kt.kblocks - 1 && kt.a_tail >= 0;
+          const CUtensorMap* am = tail ? &tmAT : &tmA;  // A: the expert's tail block from its copy
+          const int karow = tail ? kt.a_tail : krow;
           const uint32_t sa = ptx::smem_u32(stages + (size_t)stage * kStageBytes);
-          if (leader || !tail) {
-            const uint32_t full_local = ptx::smem_u32(&ctl->full[stage]);
-            if (leader) ptx::mbar_arrive_expect_tx(full_local, tail ? kStageBytes : 2 * kStageBytes);
-            const uint32_t bar = ptx::mapa(full_local, 0);
+          const uint32_t full_local = ptx::smem_u32(&ctl->full[stage]);
+          if (leader) ptx::mbar_arrive_expect_tx(full_local, 2 * kStageBytes);
+          const uint32_t bar = ptx::mapa(full_local, 0);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              ptx::tma_load_2d_pair(sa + j * kBoxBytes, &tmA, kt.row0 + 64 * j, krow, bar);
-              ptx::tma_load_2d_pair(sa + kABytes + j * kBoxBytes, &tmB, nb + 64 * j, krow, bar);
-            }
-          } else {
-            // the peer's tail block: its own barrier, so that it can zero the rows past the
-            // expert's end before telling the leader
-            const uint32_t bar = ptx::smem_u32(&ctl->pfull[stage]);
-            ptx::mbar_arrive_expect_tx(bar, kStageBytes);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              ptx::tma_load_2d(sa + j * kBoxBytes, &tmA, kt.row0 + 64 * j, krow, bar);
-              ptx::tma_load_2d(sa + kABytes + j * kBoxBytes, &tmB, nb + 64 * j, krow, bar);
-            }
+          for (int j = 0; j < 2; ++j) {
+            ptx::tma_load_2d_pair(sa + j * kBoxBytes, am, kt.row0 + 64 * j, karow, bar);
+            ptx::tma_load_2d_pair(sa + kABytes + j * kBoxBytes, &tmB, nb + 64 * j, krow, bar);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -213,61 +189,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer (leader) / tail zeroing (peer)
+    // -------------------------------------------------------------- MMA issuer (leader)
     const uint32_t idesc = ptx::idesc_bf16_f32(kMmaM, kMmaN) | (1u << 15) | (1u << 16);  // A, B MN-major
     int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0, zphase = 0;
+    uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
-    for (int tile = cid; tile < my_total && ok; tile += ncl) {
+    for (int tile = cid; leader && tile < my_total && ok; tile += ncl) {
       const KTile kt = decode_k<kKind>(s, ws, tile, m_pairs, n_tiles, M, (int)rank);
-      if (leader) {
-        ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, timeout_ns, abort_flag);
+      ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, timeout_ns, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
+      for (int kb = 0; kb < kt.kblocks; ++kb) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&ctl->full[stage]), phase, timeout_ns, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-      }
-      const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
-      for (int kb = 0; kb < kt.kblocks; ++kb) {
-        const bool tail = kb == kt.kblocks - 1 && kt.k_tail < kBK;
-        uint8_t* st_base = stages + (size_t)stage * kStageBytes;
-        if (leader) {
-          ok = ptx::mbar_wait(ptx::smem_u32(&ctl->full[stage]), phase, timeout_ns, abort_flag);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          if (tail) {
-            zero_a_tail(st_base, kt.k_tail, lane);
-            ok = ptx::mbar_wait(ptx::smem_u32(&ctl->zready[stage]), (zphase >> stage) & 1u, timeout_ns, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            zphase ^= 1u << stage;
-            if (!ok) break;
-          }
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = ptx::smem_u32(st_base);
+        if (lane == 0) {
+          const uint32_t sa = ptx::smem_u32(stages + (size_t)stage * kStageBytes);
 #pragma unroll
-            for (int ks = 0; ks < kBK / 16; ++ks)
-              ptx::mma_bf16_pair(d_tmem, desc_mnmajor_sw128(sa + ks * 2048), desc_mnmajor_sw128(sa + kABytes + ks * 2048),
-                                 idesc, (kb | ks) != 0 ? 1u : 0u);
-            ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
-          }
-          __syncwarp();
-        } else if (tail) {
-          // the peer: wait for its own tail bytes, zero, hand the block to the leader
-          ok = ptx::mbar_wait(ptx::smem_u32(&ctl->pfull[stage]), (zphase >> stage) & 1u, timeout_ns, abort_flag);
-          ok = __all_sync(0xffffffffu, ok);
-          zphase ^= 1u << stage;
-          if (!ok) break;
-          zero_a_tail(st_base, kt.k_tail, lane);
-          if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&ctl->zready[stage]), 0));
-          __syncwarp();
+          for (int ks = 0; ks < kBK / 16; ++ks)
+            ptx::mma_bf16_pair(d_tmem, desc_mnmajor_sw128(sa + ks * 2048), desc_mnmajor_sw128(sa + kABytes + ks * 2048),
+                               idesc, (kb | ks) != 0 ? 1u : 0u);
+          ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
         }
+        __syncwarp();
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      if (leader && lane == 0) ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->tfull[acc]), 0x3);
+      if (lane == 0) ptx::mma_commit_pair_multicast(ptx::smem_u32(&ctl->tfull[acc]), 0x3);
       __syncwarp();
       if (++acc == 2) {
         acc = 0;
@@ -370,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int kKind>
-cudaError_t launch_dw_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o1, const CUtensorMap& o2,
+cudaError_t launch_dw_pair(const CUtensorMap& a, const CUtensorMap& at, const CUtensorMap& b, const CUtensorMap& o1,
+                           const CUtensorMap& o2,
                            const Shape& s, const Ws& ws, int num_sms, int64_t timeout_ns, bool pdl, cudaStream_t st) {
   auto kern = gemm_dw_pair_kernel<kKind>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -392,7 +347,7 @@ cudaError_t launch_dw_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0 && 2 * clusters < grid)
       grid = 2 * clusters;
   }
-  return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, pdl, 2, a, b, o1, o2, s, ws,
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, pdl, 2, a, at, b, o1, o2, s, ws,
                        timeout_ns);
 }
 
@@ -400,21 +355,23 @@ cudaError_t launch_dw_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
 
 cudaError_t launch_gemm_dw_pair(int kind, const Shape& s, const Ws& ws, float* dw_a, float* dw_b, int num_sms,
                                 int64_t timeout_ns, bool pdl, cudaStream_t st) {
-  CUtensorMap ma, mb, mo1, mo2;
+  CUtensorMap ma, mat, mb, mo1, mo2;
   cudaError_t e;
   const uint64_t N = (uint64_t)s.N, d = (uint64_t)s.d, F = (uint64_t)s.F, E = (uint64_t)s.E;
   if (kind == kBwdDW13) {
     if ((e = make_tmap_bf16(&ma, ws.dab, N, 2 * F, 64)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mat, ws.dab_tail, E * 64, 2 * F, 64)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mb, ws.xp, N, d, 64)) != cudaSuccess) return e;
     if ((e = make_tmap_f32_rows128(&mo1, dw_a, E * F, d, 32)) != cudaSuccess) return e;
     if ((e = make_tmap_f32_rows128(&mo2, dw_b, E * F, d, 32)) != cudaSuccess) return e;
-    return launch_dw_pair<kBwdDW13>(ma, mb, mo1, mo2, s, ws, num_sms, timeout_ns, pdl, st);
+    return launch_dw_pair<kBwdDW13>(ma, mat, mb, mo1, mo2, s, ws, num_sms, timeout_ns, pdl, st);
   }
   if (kind == kBwdDW2) {
     if ((e = make_tmap_bf16(&ma, ws.dop, N, d, 64)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16(&mat, ws.dop_tail, E * 64, d, 64)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16(&mb, ws.h, N, F, 64)) != cudaSuccess) return e;
     if ((e = make_tmap_f32_rows128(&mo1, dw_a, E * d, F, 32)) != cudaSuccess) return e;
-    return launch_dw_pair<kBwdDW2>(ma, mb, mo1, mo1, s, ws, num_sms, timeout_ns, pdl, st);
+    return launch_dw_pair<kBwdDW2>(ma, mat, mb, mo1, mo1, s, ws, num_sms, timeout_ns, pdl, st);
   }
   return cudaErrorInvalidValue;
 }

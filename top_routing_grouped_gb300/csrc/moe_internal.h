@@ -65,6 +65,11 @@ struct Ws {
   void* dyp;            // [N, d] bf16: dy of each routed row
   void* dop;            // [N, d] bf16: gate * dy
   void* dab;            // [N, 2F] bf16: [dA | dB], gradients of the two pre-activations
+  // Each expert's last, partial 64-row block of dab and dop again, zero past the expert's
+  // end (block e holds rows 64e..64e+63): the weight-gradient GEMMs, whose K runs over the
+  // expert's rows, read that block from here instead of running on into the next expert.
+  void* dab_tail;       // [E * 64, 2F] bf16
+  void* dop_tail;       // [E * 64, d] bf16
   float* dgp;           // [N, 2 ceil(F/256)] partial dy . o per 128-column half tile
   void* dxslot;         // [N, d] bf16: expert-input gradient of each routed slot (token order)
   float* dlogit;        // [T, E]
@@ -78,11 +83,18 @@ struct Ws {
 struct WsLayout {
   size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
       mt_desc, pr_desc, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
-      yp, a1, a3, probs, dyp, dop, dab, dgp, dxslot, dlogit, dl_hi, dl_lo, dwr_part, dwr_part_b, total;
+      yp, a1, a3, probs, dyp, dop, dab, dab_tail, dop_tail, dgp, dxslot, dlogit, dl_hi, dl_lo, dwr_part, dwr_part_b, total;
 };
 
 // Columns of the bf16 dlogit terms: E rounded up to 64 (a whole 128-byte TMA box).
 __host__ __device__ inline int dlogit_cols(const Shape& s) { return (s.E + 63) / 64 * 64; }
+// Row of dab_tail / dop_tail that repeats routed row p of expert e (rows off .. off+cnt-1),
+// or -1 when p is not in the expert's last, partial 64-row block.
+__host__ __device__ inline int64_t tail_row(int e, int64_t p, int off, int cnt) {
+  const int whole = cnt / 64 * 64;
+  const int64_t i = p - off;
+  return (cnt % 64 != 0 && i >= whole) ? (int64_t)e * 64 + (i - whole) : -1;
+}
 constexpr int kDwrMaxChunks = 32;  // token chunks of the router-weight gradient
 
 WsLayout ws_layout(const Shape& s);

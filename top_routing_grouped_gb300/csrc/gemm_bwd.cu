@@ -5,7 +5,8 @@
 // ai-tech-blog) §3 (SwiGLU experts, gate-weighted sum) and §4 (combine / dispatch reversed):
 // for each routed row p of expert e (token t = perm_src[p], gate g = gate_perm[p]):
 //   kDH   dH'[p, f] = sum_c dy[t, c] W2_e[c, f]               (A = dYp  K-major, B = W2 MN-major)
-//         epilogue:  dg partial = sum_f h[p,f] dH'[p,f];  da = g dH' b silu'(a),  db = g dH' silu(a)
+//         epilogue:  dg partial = sum_f h[p,f] dH'[p,f];  da = g dH' b silu'(a),  db = g dH' silu(a),
+//         with h = silu(a) b recomputed from the kept a, b (not read back)
 //   kDX   dXslot[slot(p), c] = sum_f da[p,f] W1_e[f,c] + db[p,f] W3_e[f,c]
 //                                                          (A = [da|db] K-major, B = W1|W3 MN-major)
 //   kDW13 [dW1_e; dW3_e][m, c] = sum_{p in e} [da|db][p, m] Xp[p, c]   (both operands MN-major)
@@ -79,14 +80,12 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]
 // The dH epilogue's operands of one 16-column chunk of a row: h, and the two
 // pre-activations a = W1.x, b = W3.x (two 16-byte vectors each).
 struct DhChunk {
-  uint4 h[2], a[2], b[2];
+  uint4 a[2], b[2];  // W1.x and W3.x of the row (h = SiLU(a) b is recomputed from them)
 };
 
-__device__ __forceinline__ void dh_fetch(DhChunk& d, const __nv_bfloat16* hrow, const __nv_bfloat16* arow,
-                                         const __nv_bfloat16* brow, int c) {
+__device__ __forceinline__ void dh_fetch(DhChunk& d, const __nv_bfloat16* arow, const __nv_bfloat16* brow, int c) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    d.h[i] = reinterpret_cast<const uint4*>(hrow + c)[i];
     d.a[i] = reinterpret_cast<const uint4*>(arow + c)[i];
     d.b[i] = reinterpret_cast<const uint4*>(brow + c)[i];
   }
@@ -312,11 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dH: the row's h / a / b are requested a chunk ahead of their use, the first chunk
       // before the accumulator is ready, so that their latency hides behind the MMA
       const int64_t p_dh = (int64_t)bt.row0 + r;
-      const __nv_bfloat16* hrow = reinterpret_cast<const __nv_bfloat16*>(ws.h) + p_dh * s.F + n0;
       const __nv_bfloat16* arow = reinterpret_cast<const __nv_bfloat16*>(ws.a1) + p_dh * s.F + n0;
       const __nv_bfloat16* brow = reinterpret_cast<const __nv_bfloat16*>(ws.a3) + p_dh * s.F + n0;
       DhChunk pre[2];
-      if (kKind == kBwdDH && valid && n0 + c_beg < s.F) dh_fetch(pre[0], hrow, arow, brow, c_beg);
+      if (kKind == kBwdDH && valid && n0 + c_beg < s.F) dh_fetch(pre[0], arow, brow, c_beg);
       ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull[acc]), acc_phase, timeout_ns, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -333,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < (kTN / 2) / 16; ++i) {
           const int c = c_beg + 16 * i;
-          if (i + 1 < (kTN / 2) / 16 && valid && n0 + c + 16 < F) dh_fetch(pre[(i + 1) & 1], hrow, arow, brow, c + 16);
+          if (i + 1 < (kTN / 2) / 16 && valid && n0 + c + 16 < F) dh_fetch(pre[(i + 1) & 1], arow, brow, c + 16);
           if (n0 + c < F) {  // uniform across the warp
             uint32_t v[16];
             tmem_ld_16cols(t_row + c, v);
@@ -342,8 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const DhChunk& d = pre[i & 1];
 #pragma unroll
               for (int u = 0; u < 2; ++u) {
-                float hv[8], av[8], bv[8];
-                unpack8(d.h[u], hv);
+                float av[8], bv[8];
                 unpack8(d.a[u], av);
                 unpack8(d.b[u], bv);
                 uint4 oa, ob;
@@ -355,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int z = 0; z < 2; ++z) {
                     const float dh = __uint_as_float(v[8 * u + e2 + z]);
-                    dg += hv[e2 + z] * dh;
                     const float a = av[e2 + z];
                     const float sg = sigmoid_fast(a);
+                    dg += a * sg * bv[e2 + z] * dh;  // h = SiLU(a) b, recomputed
                     da[z] = g * dh * bv[e2 + z] * sg * (1.0f + a * (1.0f - sg));
                     db[z] = g * dh * a * sg;
                   }

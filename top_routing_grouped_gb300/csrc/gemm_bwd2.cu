@@ -4,7 +4,8 @@
 // Backward of "Distributed Training Part 4 ... MoE + Expert Parallelism" (jesamkim
 // ai-tech-blog) §3 (SwiGLU experts, gate-weighted sum), for each routed row p of expert e:
 //   kDH  dH'[p, f] = sum_c dy[t, c] W2_e[c, f]        (A = dYp K-major, B = W2 MN-major)
-//        epilogue: dg partial = sum_f h[p,f] dH'[p,f];  da = g dH' b silu'(a),  db = g dH' silu(a)
+//        epilogue: dg partial = sum_f h[p,f] dH'[p,f];  da = g dH' b silu'(a),  db = g dH' silu(a),
+//        with h = silu(a) b recomputed from the kept a, b (not read back)
 //   kDX  dXslot[slot(p), c] = sum_f da[p,f] W1_e[f,c] + db[p,f] W3_e[f,c]
 //                                                   (A = [da|db] K-major, B = W1|W3 MN-major)
 // A cluster of two CTAs computes a 256 x 256 tile: each CTA loads its own 128 rows of A and
@@ -68,7 +69,7 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kEp
 // the warp's 32 and on the 8 columns 8 (l % 4) .. of the 32-column chunk; these are the
 // rows' h, a = W1.x and b = W3.x there (one 16-byte vector each).
 struct DhIn {
-  uint4 h[4], a[4], b[4];
+  uint4 a[4], b[4];  // W1.x and W3.x of the row (h = SiLU(a) b is recomputed from them)
 };
 
 
@@ -252,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the h / a / b vectors of row group i of chunk c (columns n0 + c + cg ..)
       auto fetch_row = [&](int i, int c) {
         const int64_t off = prow[i] * s.F + n0 + c + cg;
-        in.h[i] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(ws.h) + off);
         in.a[i] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(ws.a1) + off);
         in.b[i] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(ws.a3) + off);
       };
@@ -302,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ld_block_v4(xb + (uint32_t)br * 128u + (uint32_t)((((cg >> 2) + 1) ^ (br & 7)) * 16), dh[4], dh[5], dh[6],
                          dh[7]);
             if (rv[i]) {
-              float hv[8], av[8], bv[8];
-              unpack8(in.h[i], hv);
+              float av[8], bv[8];
               unpack8(in.a[i], av);
               unpack8(in.b[i], bv);
               if (has_next) fetch_row(i, c + 32);
@@ -316,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int z = 0; z < 2; ++z) {
                   const float d = dh[e2 + z];
-                  dgacc[i] += hv[e2 + z] * d;
                   const float a = av[e2 + z];
                   const float sg = sigmoid_fast(a);
+                  dgacc[i] += a * sg * bv[e2 + z] * d;  // h = SiLU(a) b, recomputed
                   da[z] = g[i] * d * bv[e2 + z] * sg * (1.0f + a * (1.0f - sg));
                   db[z] = g[i] * d * a * sg;
                 }

@@ -97,65 +97,92 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_dy_kernel(Shape s, W
   }
 }
 
-// One thread per token: dlogit[t, :] (fp32).
+// dlogit[t, :] for a block of 128 tokens, one thread per token.  The block's softmax rows are
+// staged in shared memory with coalesced loads (rows padded to E + 1 floats, so the threads'
+// row walks hit 32 different banks), each thread turns its row into dlogit in place, and the
+// block writes dlogit (fp32) and its two bf16 terms with coalesced stores.
+//   dp[e] = c_e + delta_e,  c_e = alpha E f_e / T (balancing loss),  delta_e = the gradient of
+//   the loss through gate j when e = idx[t, j] (renormalised gates: (dg_j - sum_i g_i dg_i) / S);
+//   dlogit[e] = p[e] (dp[e] - sum_e' p[e'] dp[e']) / tau  (softmax backward, temperature tau).
+template <int KS>  // top-k capacity of the per-thread arrays (k <= KS)
 __global__ void __launch_bounds__(128) router_bwd_kernel(Shape s, Ws ws, float alpha, int n_tiles_dh) {
-  extern __shared__ float dp_s[];  // [128][E+1]
+  extern __shared__ float smem_f[];
+  const int E = s.E, k = s.k, ldp = E + 1;
+  float* c_s = smem_f;        // [E] balancing-loss term of each expert
+  float* p_s = smem_f + E;    // [128][E + 1] softmax rows, then dlogit rows
   const int r = threadIdx.x;
-  const int64_t t = (int64_t)blockIdx.x * 128 + r;
-  const int E = s.E, k = s.k;
+  const int64_t t0 = (int64_t)blockIdx.x * 128;
+  const int rows = (int)(s.T - t0 < 128 ? s.T - t0 : 128);
   pdl_wait();
   pdl_launch_dependents();
-  if (t >= s.T) return;
-  float* dp = dp_s + r * (E + 1);
-  // balancing-loss term: d(alpha * aux)/dp[t,e] = alpha * E * f_e / T
-  for (int e = 0; e < E; ++e) dp[e] = alpha * (float)E * ((float)ws.counts[e] / ((float)s.T * (float)k)) / (float)s.T;
-  const float* pt = ws.probs + t * E;
-  float dg[kMaxTopK];
-  float gdg = 0.f, S = 0.f;
+  for (int e = r; e < E; e += 128) c_s[e] = alpha * (float)E * ((float)ws.counts[e] / ((float)s.T * (float)k)) / (float)s.T;
+  const float* pg = ws.probs + t0 * E;
+  for (int i = r; i < rows * E; i += 128) p_s[(i / E) * ldp + i % E] = pg[i];
+  __syncthreads();
+  if (r < rows) {
+    const int64_t t = t0 + r;
+    float* pr = p_s + r * ldp;
+    int idx[KS];
+    float dg[KS], pe[KS];
+    float gdg = 0.f, S = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    dg[j] = 0.f;
-    if (j >= k) continue;
-    const int64_t p = ws.slot_pos[t * k + j];
-    if (p >= 0 && p < s.N)
-      for (int n = 0; n < n_tiles_dh; ++n) dg[j] += ws.dgp[p * n_tiles_dh + n];  // tiles in order
-    const int e = ws.topk_idx[t * k + j];
-    if (e < 0 || e >= E) continue;
-    gdg += ws.topk_gate[t * k + j] * dg[j];
-    S += pt[e];
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j >= k) continue;
-    const int e = ws.topk_idx[t * k + j];
-    if (e < 0 || e >= E) continue;
-    dp[e] += s.renorm ? (dg[j] - gdg) / S : dg[j];  // renormalised gates: g_j = p_j / S
-  }
-  float pdp = 0.f;
-  for (int e = 0; e < E; ++e) pdp += pt[e] * dp[e];
-  // dlogit in fp32, and as two bf16 terms for the tensor-core router-weight gradient
-  const int ec = dlogit_cols(s);  // a multiple of 64: whole 16-byte vectors of 8
-  uint4* hi = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.dl_hi) + t * ec);
-  uint4* lo = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(ws.dl_lo) + t * ec);
-  for (int e0 = 0; e0 < ec; e0 += 8) {
-    uint4 vh, vl;
-    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&vh);
-    __nv_bfloat162* l2 = reinterpret_cast<__nv_bfloat162*>(&vl);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float v[2];
-#pragma unroll
-      for (int z = 0; z < 2; ++z) {
-        const int e = e0 + 2 * u + z;
-        v[z] = e < E ? pt[e] * (dp[e] - pdp) / s.tau : 0.f;
-        if (e < E) ws.dlogit[t * E + e] = v[z];
-      }
-      h2[u] = __floats2bfloat162_rn(v[0], v[1]);
-      const float2 hf = __bfloat1622float2(h2[u]);
-      l2[u] = __floats2bfloat162_rn(v[0] - hf.x, v[1] - hf.y);
+    for (int j = 0; j < KS; ++j) {
+      dg[j] = 0.f;
+      idx[j] = -1;
+      pe[j] = 0.f;
+      if (j >= k) continue;
+      const int64_t p = ws.slot_pos[t * k + j];
+      if (p >= 0 && p < s.N)
+        for (int n = 0; n < n_tiles_dh; ++n) dg[j] += ws.dgp[p * n_tiles_dh + n];  // tiles in order
+      const int e = ws.topk_idx[t * k + j];
+      if (e < 0 || e >= E) continue;
+      idx[j] = e;
+      pe[j] = pr[e];
+      gdg += ws.topk_gate[t * k + j] * dg[j];
+      S += pe[j];
     }
-    hi[e0 / 8] = vh;
-    lo[e0 / 8] = vl;
+    // delta of each chosen expert, and sum_e p[e] dp[e] in expert order
+#pragma unroll
+    for (int j = 0; j < KS; ++j)
+      if (j < k) dg[j] = s.renorm ? (dg[j] - gdg) / S : dg[j];
+    float pdp = 0.f;
+    for (int e = 0; e < E; ++e) {
+      float dp = c_s[e];
+#pragma unroll
+      for (int j = 0; j < KS; ++j)
+        if (j < k && idx[j] == e) dp += dg[j];
+      pdp += pr[e] * dp;
+    }
+    for (int e = 0; e < E; ++e) pr[e] = pr[e] * (c_s[e] - pdp) / s.tau;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {  // the chosen experts add their delta (once per expert)
+      if (j >= k || idx[j] < 0) continue;
+      float dp = c_s[idx[j]];
+      bool first = true;
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        if (i >= k || idx[i] != idx[j]) continue;
+        if (i < j) first = false;
+        dp += dg[i];
+      }
+      if (first) pr[idx[j]] = pe[j] * (dp - pdp) / s.tau;
+    }
+  }
+  __syncthreads();
+  // dlogit in fp32, and as two bf16 terms (columns past E zero) for the tensor-core products
+  float* dl = ws.dlogit + t0 * E;
+  for (int i = r; i < rows * E; i += 128) dl[i] = p_s[(i / E) * ldp + i % E];
+  const int ec = dlogit_cols(s);  // a multiple of 64
+  __nv_bfloat162* hi = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(ws.dl_hi) + t0 * ec);
+  __nv_bfloat162* lo = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(ws.dl_lo) + t0 * ec);
+  for (int i = r; i < rows * (ec / 2); i += 128) {
+    const int row = i / (ec / 2), e = 2 * (i % (ec / 2));
+    const float v0 = e < E ? p_s[row * ldp + e] : 0.f;
+    const float v1 = e + 1 < E ? p_s[row * ldp + e + 1] : 0.f;
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    hi[i] = h;
+    lo[i] = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
   }
 }
 
@@ -199,10 +226,12 @@ cudaError_t launch_gather_dy(const Shape& s, const Ws& ws, const void* dy, int n
 }
 
 cudaError_t launch_router_bwd(const Shape& s, const Ws& ws, float alpha, int n_tiles_dh, bool pdl, cudaStream_t st) {
-  const size_t smem = sizeof(float) * 128 * (size_t)(s.E + 1);
-  cudaError_t e = cudaFuncSetAttribute(router_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(float) * ((size_t)s.E + 128 * (size_t)(s.E + 1));
+  auto kern = s.k <= 2 ? router_bwd_kernel<2> : s.k <= 4 ? router_bwd_kernel<4>
+                                             : s.k <= 8 ? router_bwd_kernel<8> : router_bwd_kernel<kMaxTopK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(router_bwd_kernel, dim3((unsigned)s.nblk), dim3(128), smem, st, pdl, 1, s, ws, alpha, n_tiles_dh);
+  return launch_kernel(kern, dim3((unsigned)s.nblk), dim3(128), smem, st, pdl, 1, s, ws, alpha, n_tiles_dh);
 }
 
 cudaError_t launch_dwr_reduce(const Shape& s, const Ws& ws, float* dwr, float* dbias, int num_sms, bool pdl,

@@ -188,15 +188,29 @@ __global__ void __launch_bounds__(128) router_bwd_kernel(Shape s, Ws ws, float a
 
 // The router-bias gradient of each router block: part_b[blk, e] = sum over the block's
 // tokens of dlogit[t, e], in token order.
+// Sum of n values strided by `stride`, in index order; the loads of each group of 8 are issued
+// together so that their latencies overlap (the additions keep the sequential order).
+__device__ __forceinline__ float ordered_sum(const float* p, int64_t stride, int n) {
+  float v = 0.f;
+  int i = 0;
+  for (; i + 8 <= n; i += 8) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = p[(int64_t)(i + u) * stride];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v += x[u];
+  }
+  for (; i < n; ++i) v += p[(int64_t)i * stride];
+  return v;
+}
+
 __global__ void __launch_bounds__(128) dbias_block_kernel(Shape s, Ws ws) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t t0 = (int64_t)blockIdx.x * 128;
-  for (int e = threadIdx.x; e < s.E; e += 128) {
-    float v = 0.f;
-    for (int r = 0; r < 128 && t0 + r < s.T; ++r) v += ws.dlogit[(t0 + r) * s.E + e];
-    ws.dwr_part_b[(int64_t)blockIdx.x * s.E + e] = v;
-  }
+  const int rows = (int)(s.T - t0 < 128 ? s.T - t0 : 128);
+  for (int e = threadIdx.x; e < s.E; e += 128)
+    ws.dwr_part_b[(int64_t)blockIdx.x * s.E + e] = ordered_sum(ws.dlogit + t0 * s.E + e, s.E, rows);
 }
 
 // dW_r = sum of the token-chunk partials in chunk order; dbias = sum of the router-block
@@ -206,17 +220,10 @@ __global__ void __launch_bounds__(256) dwr_reduce_kernel(Shape s, const float* p
   pdl_wait();
   pdl_launch_dependents();
   const int64_t n = (int64_t)s.E * s.d;
-  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
-    float v = 0.f;
-    for (int ch = 0; ch < chunks; ++ch) v += part[(int64_t)ch * n + i];
-    dwr[i] = v;
-  }
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256)
+    dwr[i] = ordered_sum(part + i, n, chunks);
   if (dbias && blockIdx.x == 0)
-    for (int e = threadIdx.x; e < s.E; e += 256) {
-      float v = 0.f;
-      for (int b = 0; b < s.nblk; ++b) v += part_b[(int64_t)b * s.E + e];
-      dbias[e] = v;
-    }
+    for (int e = threadIdx.x; e < s.E; e += 256) dbias[e] = ordered_sum(part_b + e, s.E, s.nblk);
 }
 
 cudaError_t launch_gather_dy(const Shape& s, const Ws& ws, const void* dy, int num_sms, bool pdl, cudaStream_t st) {

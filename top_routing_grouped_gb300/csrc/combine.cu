@@ -4,7 +4,10 @@
 // §3 output formula y = sum_{i in TopK} G(x)_i E_i(x) (the gate factor is already applied
 // by the down-projection epilogue) and §4 Combine (expert outputs return to their token:
 // Yp holds them in expert order, slot_pos[t*k + j] is the row of token t's j-th choice).
-// A fixed summation order keeps y bit-reproducible (no float atomics).
+// A fixed summation order keeps y bit-reproducible (no float atomics).  A slot_pos entry
+// outside the routed rows (a corrupt permutation) is clamped into them for the read and
+// reported (MOE_ERR_INTERNAL, site 0x600 / 0x601) once per thread after its loop, so that
+// the check adds no branch to the gather itself.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -19,6 +22,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws 
   const int vec_per_row = s.d / 8;
   const int64_t total = s.T * (int64_t)vec_per_row;
   const int4* ys = reinterpret_cast<const int4*>(ws.yp);
+  bool bad = false;
   pdl_wait();  // the down-projection's rows
   pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
@@ -30,7 +34,9 @@ __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws 
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
     for (int j = 0; j < s.k; ++j) {
       // clamped into the routed rows, so that not even a corrupt permutation reads outside Yp
-      const int64_t row = min((uint32_t)__ldg(&ws.slot_pos[t * s.k + j]), (uint32_t)(s.N - 1));
+      const uint32_t sp = (uint32_t)__ldg(&ws.slot_pos[t * s.k + j]);
+      bad |= sp >= (uint32_t)s.N;
+      const int64_t row = min(sp, (uint32_t)(s.N - 1));
       int4 raw = __ldcs(ys + row * vec_per_row + v);
       const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -52,6 +58,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_bf16_kernel(Shape s, Ws 
       yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
+  if (bad) record_error(ws, MOE_ERR_INTERNAL, 0x600u);
 }
 
 // fp32 slots -> fp32 or bf16 y; 4 columns per thread-step.
@@ -60,6 +67,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
   const int vec_per_row = s.d / 4;
   const int64_t total = s.T * (int64_t)vec_per_row;
   const float4* ys = reinterpret_cast<const float4*>(ws.yp);
+  bool bad = false;
   pdl_wait();
   pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * kCombThreads + threadIdx.x; i < total;
@@ -68,7 +76,9 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
     const int v = (int)(i % vec_per_row);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < s.k; ++j) {
-      const int64_t row = min((uint32_t)__ldg(&ws.slot_pos[t * s.k + j]), (uint32_t)(s.N - 1));  // clamped
+      const uint32_t sp = (uint32_t)__ldg(&ws.slot_pos[t * s.k + j]);
+      bad |= sp >= (uint32_t)s.N;
+      const int64_t row = min(sp, (uint32_t)(s.N - 1));  // clamped
       const float4 f = ys[row * vec_per_row + v];
       acc.x += f.x;
       acc.y += f.y;
@@ -83,6 +93,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_f32_kernel(Shape s, Ws w
       reinterpret_cast<float4*>(w.y)[t * vec_per_row + v] = acc;
     }
   }
+  if (bad) record_error(ws, MOE_ERR_INTERNAL, 0x601u);
 }
 
 cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st) {

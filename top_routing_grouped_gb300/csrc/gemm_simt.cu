@@ -8,7 +8,7 @@
 // slot t*k+j, summed per token by the combine kernel).
 //
 //   GEMM1 (kMode = 1): H[p, f]         = SiLU(Xp[p] . W1_e[f]) * (Xp[p] . W3_e[f])
-//   GEMM2 (kMode = 2): Yslot[slot(p), c] = gate(p) * (H[p] . W2_e[c])
+//   GEMM2 (kMode = 2): Yp[p, c] = gate(p) * (H[p] . W2_e[c])   (row p in expert order)
 // for every row p of expert e, over the tile table built by the scan kernel.
 #include <cuda_bf16.h>
 

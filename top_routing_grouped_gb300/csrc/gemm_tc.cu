@@ -9,7 +9,7 @@
 // "Compute-Optimal Is Not Cluster-Optimal" (operator-level performance model).
 //
 //   mode 1:  H[p, n]          = SiLU(Xp[p] . W1_e[n]) * (Xp[p] . W3_e[n])   (MMA N = 128 + 128)
-//   mode 2:  Yslot[slot(p), n] = gate(p) * (H[p] . W2_e[n])                   (MMA N = 256)
+//   mode 2:  Yp[p, n] = gate(p) * (H[p] . W2_e[n]), row p in expert order          (MMA N = 256)
 //
 // Work: the tile table of the scan kernel (m-tiles of 128 rows of one expert, grouped so
 // that CTAs running together share weight tiles in L2) times the n-tiles.  Every CTA

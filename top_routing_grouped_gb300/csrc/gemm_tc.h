@@ -25,7 +25,7 @@ cudaError_t launch_gemm_bwd(int kind, const Shape& s, const Ws& ws, const Weight
 
 cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int num_sms, int64_t timeout_ns,
                             cudaStream_t st);
-// mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yslot[slot] = gate * (H W2^T)
+// mode 1: H = SiLU(Xp W1^T) * (Xp W3^T); mode 2: Yp = gate * (H W2^T) (expert order)
 cudaError_t launch_gemm_tc(int mode, const Shape& s, const Ws& ws, const Weights& w, int num_sms,
                            int64_t timeout_ns, bool test_stall, bool pdl, cudaStream_t st);
 

@@ -3,7 +3,8 @@
 // Same operation as gemm_tc.cu (after "Distributed Training Part 4 ... MoE + Expert
 // Parallelism", jesamkim ai-tech-blog, §3 Structure / output formula, §4 Combine):
 //   mode 1:  H[p, n]           = SiLU(Xp[p] . W1_e[n]) * (Xp[p] . W3_e[n])
-//   mode 2:  Yslot[slot(p), n] = gate(p) * (H[p] . W2_e[n])
+//   mode 2:  Yp[p, n]          = gate(p) * (H[p] . W2_e[n])   (row p in expert order, like Xp
+//                                and H; the combine gathers token t's rows through slot_pos)
 //
 // A cluster of two CTAs on two SMs computes a 256 x 256 tile with one MMA stream issued by
 // the first CTA (the leader): each CTA loads only its own 128 rows of A and its half of the

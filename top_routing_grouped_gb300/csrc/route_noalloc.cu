@@ -27,13 +27,18 @@ constexpr size_t kNoAllocScratchBytes = (size_t)MOE_NOALLOC_SCRATCH_BYTES;
 constexpr int kChunk = 32;     // columns of d per shared-memory step of the logit loop
 constexpr int kMaxDevices = 64;
 
-// Scratch layout: [0, 256) ticket + status words; then the per-slot local ranks
-// [T*k] int32, the per-block counts [nblk*E] int32 and softmax sums [nblk*E] fp32.
+// Scratch layout: [0, 256) the status header (the 64 words a workspace header has: the
+// status word, the failure site, ...); [256, 512) the completion ticket; then the per-slot
+// local ranks [T*k] int32, the per-block counts [nblk*E] int32 and softmax sums
+// [nblk*E] fp32, each region starting on a 256-byte boundary.
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
+constexpr size_t kTicketAt = 256, kRanksAt = 512;
+static_assert(kTicketAt >= 64 * sizeof(uint32_t), "the status header holds 64 words");
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t scratch_needed(const Shape& s) {
-  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  return 256 + up((size_t)s.N * 4) + 2 * up((size_t)s.nblk * s.E * 4);
+  return kRanksAt + up256((size_t)s.N * 4) + 2 * up256((size_t)s.nblk * s.E * 4);
 }
 
 // Device address of g_route_scratch on each device, looked up once per device with that
@@ -60,8 +65,11 @@ void* scratch_address(int device, cudaError_t* err) {
 // counting in route_finish) followed by a last-block reduction: the block that finishes
 // last sums the per-block counts and softmax sums in block order and writes the expert
 // counts and aux = E * sum_e f_e P_e, with the same summation order as the scan kernel.
+// The last block also copies the status word (0, or the first error any block recorded:
+// MOE_ERR_INTERNAL for a NaN logit) to *status_out.
 __global__ void __launch_bounds__(kRouteBlock) route_noalloc_kernel(Shape s, Ws ws, Weights w, uint32_t* ticket,
-                                                                    int32_t* counts_out, float* aux_out) {
+                                                                    int32_t* counts_out, float* aux_out,
+                                                                    uint32_t* status_out) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int ldz = s.E + 1;
   float* z_s = reinterpret_cast<float*>(smem_raw);                       // [128][E+1]
@@ -129,7 +137,10 @@ __global__ void __launch_bounds__(kRouteBlock) route_noalloc_kernel(Shape s, Ws 
     for (int e = r; e < half; e += kRouteBlock) red[e] += red[e + half];
     __syncthreads();
   }
-  if (r == 0) *aux_out = (float)s.E * red[0];
+  if (r == 0) {
+    *aux_out = (float)s.E * red[0];
+    *status_out = __ldcg(&ws.hdr[kHdrStatus]);
+  }
 }
 
 thread_local char g_msg[256];
@@ -139,15 +150,22 @@ thread_local char g_msg[256];
 
 extern "C" moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const void* w_router, const float* router_bias,
                                         int32_t* topk_idx, float* topk_gate, int32_t* expert_counts, float* aux,
-                                        void* stream) {
+                                        uint32_t* device_status, void* stream) {
   using namespace moe;
-  if (!plan || !x || !w_router || !topk_idx || !topk_gate || !expert_counts || !aux) {
+  // every argument check comes before the first CUDA call
+  if (!plan || !x || !w_router || !topk_idx || !topk_gate || !expert_counts || !aux || !device_status) {
     snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: null argument");
     return set_last_error(MOE_ERR_INVALID_ARG, g_msg);
   }
+  const void* ptrs[] = {x, w_router, topk_idx, topk_gate, expert_counts, aux, device_status};
+  for (const void* p : ptrs)
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) {
+      snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: every device pointer must be 16-byte aligned");
+      return set_last_error(MOE_ERR_INVALID_ARG, g_msg);
+    }
   Shape s = *plan_shape(plan);
-  if (s.has_bias && !router_bias) {
-    snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: the plan has a router bias but router_bias is null");
+  if (s.has_bias && (!router_bias || reinterpret_cast<uintptr_t>(router_bias) % 16 != 0)) {
+    snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: the plan has a router bias: router_bias must be a 16-byte aligned pointer");
     return set_last_error(MOE_ERR_INVALID_ARG, g_msg);
   }
   const size_t need = scratch_needed(s);
@@ -158,6 +176,12 @@ extern "C" moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const vo
              need, kNoAllocScratchBytes);
     return set_last_error(MOE_ERR_UNSUPPORTED, g_msg);
   }
+  // Only routing runs here: whatever else a plan's flags ask the forward to keep (logits,
+  // the softmax a training plan keeps for its backward) has no place in the scratch and is
+  // switched off, so that no store is gated on a region this call does not have.
+  s.keep_logits = 0;
+  s.training = 0;
+
   int dev = 0;
   unsigned char* base = nullptr;
   cudaError_t e = cudaGetDevice(&dev);
@@ -166,21 +190,18 @@ extern "C" moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const vo
     snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: looking up the scratch buffer: %s", cudaGetErrorString(e));
     return set_last_error(MOE_ERR_CUDA, g_msg);
   }
-  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
   Ws ws{};
-  ws.hdr = reinterpret_cast<uint32_t*>(base + 64);
-  ws.local_rank = reinterpret_cast<int32_t*>(base + 256);
-  ws.blk_cnt = reinterpret_cast<int32_t*>(base + 256 + up((size_t)s.N * 4));
-  ws.blk_psum = reinterpret_cast<float*>(base + 256 + up((size_t)s.N * 4) + up((size_t)s.nblk * s.E * 4));
+  ws.hdr = reinterpret_cast<uint32_t*>(base);
+  ws.local_rank = reinterpret_cast<int32_t*>(base + kRanksAt);
+  ws.blk_cnt = reinterpret_cast<int32_t*>(base + kRanksAt + up256((size_t)s.N * 4));
+  ws.blk_psum = reinterpret_cast<float*>(base + kRanksAt + up256((size_t)s.N * 4) + up256((size_t)s.nblk * s.E * 4));
   ws.topk_idx = topk_idx;
   ws.topk_gate = topk_gate;
-  ws.logits = nullptr;
-  s.keep_logits = 0;
   Weights w{x, w_router, s.has_bias ? router_bias : nullptr, nullptr, nullptr, nullptr, nullptr};
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the ticket and the status words must start at zero on every call
-  if ((e = cudaMemsetAsync(base, 0, 256, st)) != cudaSuccess) {
+  // the status header and the ticket must start at zero on every call
+  if ((e = cudaMemsetAsync(base, 0, kRanksAt, st)) != cudaSuccess) {
     snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: clearing the scratch header: %s", cudaGetErrorString(e));
     return set_last_error(MOE_ERR_CUDA, g_msg);
   }
@@ -189,8 +210,8 @@ extern "C" moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const vo
                       sizeof(uint32_t) * (4 * (size_t)s.E + 2 * kRouteBlock);
   if ((e = cudaFuncSetAttribute(route_noalloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) ==
       cudaSuccess) {
-    route_noalloc_kernel<<<s.nblk, kRouteBlock, smem, st>>>(s, ws, w, reinterpret_cast<uint32_t*>(base), expert_counts,
-                                                            aux);
+    route_noalloc_kernel<<<s.nblk, kRouteBlock, smem, st>>>(s, ws, w, reinterpret_cast<uint32_t*>(base + kTicketAt),
+                                                            expert_counts, aux, device_status);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

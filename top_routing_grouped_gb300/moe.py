@@ -69,7 +69,7 @@ _lib.moe_backward_stage_count.argtypes = [_P]
 _lib.moe_backward_stage_count.restype = ctypes.c_int32
 _lib.moe_backward_stage_name.argtypes = [_P, ctypes.c_int32]
 _lib.moe_backward_stage_name.restype = ctypes.c_char_p
-_lib.moe_route_noalloc.argtypes = [_P] * 8 + [_P]
+_lib.moe_route_noalloc.argtypes = [_P] * 9 + [_P]
 _lib.moe_route_noalloc.restype = ctypes.c_int
 _lib.moe_last_error.argtypes = []
 _lib.moe_last_error.restype = ctypes.c_char_p
@@ -188,11 +188,13 @@ class MoEPlan:
         _check(_lib.moe_aux_loss(self._h, _ptr(workspace), _ptr(out), _stream(stream)), "moe_aux_loss")
         return out
 
-    def route_noalloc(self, x, w_router, bias, topk_idx, topk_gate, expert_counts, aux, stream=None):
+    def route_noalloc(self, x, w_router, bias, topk_idx, topk_gate, expert_counts, aux, device_status, stream=None):
         """Routing only, with the library's static scratch (moe_route_noalloc): for callers
-        that cannot allocate device memory.  All outputs are caller-provided tensors."""
+        that cannot allocate device memory.  All outputs are caller-provided tensors;
+        device_status (one int32/uint32 element) receives 0 or the error a kernel recorded."""
         _check(_lib.moe_route_noalloc(self._h, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
-                                      _ptr(topk_gate), _ptr(expert_counts), _ptr(aux), _stream(stream)),
+                                      _ptr(topk_gate), _ptr(expert_counts), _ptr(aux), _ptr(device_status),
+                                      _stream(stream)),
                "moe_route_noalloc")
 
     def device_status(self, workspace, stream=None):

@@ -1,9 +1,10 @@
 """Benchmark of the sparse-MoE forward on GB300 (one JSON line on stdout, rank 0).
 
-Workload (default): the coarse-expert layer, T=4096 tokens, d_model=2048, E=8 experts, top-2,
-d_expert=8192, bf16 inputs, seeded synthetic data.  A step is one whole forward (router,
-scan, permute, grouped SwiGLU GEMM, grouped down-projection with gate and un-permute,
-combine, balancing scalar) through the C ABI.
+Workload (default): the large layer, T=32768 tokens, d_model=4096, E=64 experts, top-4,
+d_expert=2048, router temperature 0.5, bf16 inputs, seeded synthetic data (the largest of the
+listed layers; --workload picks another).  A step is one whole forward (router, scan, permute,
+grouped SwiGLU GEMM, grouped down-projection with gate and un-permute, combine, balancing
+scalar) through the C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -38,7 +39,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="coarse_e8")
+    ap.add_argument("--workload", default="large_e64")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling a smaller case)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -102,13 +103,15 @@ def kernel_source_digest(kernel):
 
 def recorded_traffic(workload, kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current kernel sources (else None).  The summary gives either the full-size launch's
+    bytes, or (for layers too large to capture whole) the bytes extrapolated to the full
+    launch from captures at reduced T, with the fit it used."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.ncu.txt")
     if not os.path.exists(path):
         return None
     vals = {}
     for line in open(path):
-        if ":" in line:
+        if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
     if vals.get("kernel_sources") != kernel_source_digest(kernel):

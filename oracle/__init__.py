@@ -39,12 +39,13 @@ def load(path=None):
     lib.orc_router.argtypes = [cfgp, P, P, P, P, P, P, P]
     lib.orc_dispatch.argtypes = [cfgp, P, P, P, P, P]
     lib.orc_expert.argtypes = [cfgp, P, P, P, P, ctypes.c_int64, ctypes.c_int32, P, P]
+    lib.orc_expert_rows.argtypes = [cfgp, P, P, P, P, ctypes.c_int64, P, P, P, P]
     lib.orc_combine.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_int64, P]
     lib.orc_aux.argtypes = [cfgp, P, P, P]
     lib.orc_forward.argtypes = [cfgp] + [P] * 16
     lib.orc_backward.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_double, P, P, P, P, P, P]
     lib.orc_num_threads.argtypes = []
-    for f in ("orc_router", "orc_dispatch", "orc_expert", "orc_combine", "orc_aux",
+    for f in ("orc_router", "orc_dispatch", "orc_expert", "orc_expert_rows", "orc_combine", "orc_aux",
               "orc_forward", "orc_num_threads", "orc_backward"):
         getattr(lib, f).restype = ctypes.c_int
     if path is None or path == _build.LIB:
@@ -119,6 +120,20 @@ class Oracle:
         self._call("orc_expert", self._p(self._in(x)), self._p(self._in(w1)),
                    self._p(self._in(w3)), self._p(self._in(w2)), int(t), int(e),
                    self._p(h), self._p(out))
+        return h, out
+
+    def expert_rows(self, x, w1, w3, w2, tokens, experts, want_h=True):
+        """Row i: (h [F], out [d]) of expert experts[i] on token tokens[i] (fp64), as
+        ``expert`` computes one; returns (h [n, F] or None, out [n, d])."""
+        tk = np.ascontiguousarray(tokens, dtype=np.int64)
+        ex = np.ascontiguousarray(experts, dtype=np.int32)
+        if tk.shape != ex.shape or tk.ndim != 1:
+            raise ValueError("tokens and experts must be 1-D and of one length")
+        n = tk.size
+        h = np.empty((n, self.F), np.float64) if want_h else None
+        out = np.empty((n, self.d), np.float64)
+        self._call("orc_expert_rows", self._p(self._in(x)), self._p(self._in(w1)), self._p(self._in(w3)),
+                   self._p(self._in(w2)), n, self._p(tk), self._p(ex), self._p(h), self._p(out))
         return h, out
 
     def combine(self, x, w1, w3, w2, idx, gate, tokens=None):

@@ -225,6 +225,38 @@ int orc_expert(const orc_cfg* c, const void* x, const void* w1, const void* w3, 
   return ORC_OK;
 }
 
+/* Many (token, expert) evaluations at once, for checking many routed rows: row i is expert
+ * e[i] applied to token t[i], exactly as orc_expert computes it (the same per-row
+ * arithmetic, rows independent, so the OpenMP loop over rows changes no result).
+ * h_out [n, F] may be NULL; out [n, d] receives the expert outputs. */
+int orc_expert_rows(const orc_cfg* c, const void* x, const void* w1, const void* w3, const void* w2, int64_t n,
+                    const int64_t* t, const int32_t* e, double* h_out, double* out) {
+  if (orc_check(c) || !x || !w1 || !w3 || !w2 || !t || !e || !out || n < 0) return ORC_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i)
+    if (t[i] < 0 || t[i] >= c->T || e[i] < 0 || e[i] >= c->E) return ORC_BAD_ARG;
+  const int32_t d = c->d, F = c->F;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+    double* h = (double*)malloc(sizeof(double) * (size_t)F);
+    if (!xr || !h) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t i = 0; i < n; ++i) {
+        for (int32_t col = 0; col < d; ++col) xr[col] = orc_load(x, c->dtype, t[i] * d + col);
+        orc_expert_row(c, w1, w3, w2, e[i], xr, h, out + i * d);
+        if (h_out) memcpy(h_out + i * F, h, sizeof(double) * (size_t)F);
+      }
+    }
+    free(xr);
+    free(h);
+  }
+  return failed ? ORC_NO_MEM : ORC_OK;
+}
+
 /*
  * Combine (§3 output formula; §4 Combine: expert outputs return to their token):
  *   y[i] = sum_{j=0..k-1} gate[t,j] * E_{idx[t,j]}(x[t]),   t = tokens[i]
@@ -354,7 +386,7 @@ int orc_num_threads(void) {
  *     dz = p * (dp - sum_e p_e dp_e),  dl = dz / tau
  *     dW_r[e] += dl_e x,  dbias_e += dl_e,  dx += sum_e dl_e W_r[e]
  * Outputs (host, fp64): dx [T,d], dwr [E,d], dbias [E], dw1, dw3 [E,F,d], dw2 [E,d,F].
- * Weight gradients are summed over tokens in token order (OpenMP over experts).
+ * Weight gradients are summed over tokens in token order (OpenMP over output rows).
  */
 int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* bias, const void* w1, const void* w3,
                  const void* w2, const double* dy, double alpha, double* dx, double* dwr, double* dbias,
@@ -372,10 +404,11 @@ int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* b
   double* sb = (double*)malloc(sizeof(double) * (size_t)(N * F)); /* db */
   double* sh = (double*)malloc(sizeof(double) * (size_t)(N * F)); /* h */
   double* dg = (double*)malloc(sizeof(double) * (size_t)N);
+  int32_t* perm = (int32_t*)malloc(sizeof(int32_t) * (size_t)N); /* slot of each dispatched row */
   int rc = ORC_OK;
-  if (!p || !idx || !gate || !counts || !offsets || !sa || !sb || !sh || !dg) rc = ORC_NO_MEM;
+  if (!p || !idx || !gate || !counts || !offsets || !sa || !sb || !sh || !dg || !perm) rc = ORC_NO_MEM;
   if (!rc) rc = orc_router(c, x, wr, bias, NULL, p, idx, gate);
-  if (!rc) rc = orc_dispatch(c, idx, counts, offsets, NULL, NULL);
+  if (!rc) rc = orc_dispatch(c, idx, counts, offsets, NULL, perm);
   int failed = 0;
   if (!rc) {
 #pragma omp parallel
@@ -421,11 +454,10 @@ int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* b
               dgs += dyt[r] * acc;
             }
             dg[slot] = dgs;
-            for (int32_t f = 0; f < F; ++f) {
-              double acc = 0.0;
-              for (int32_t r = 0; r < d; ++r) acc += orc_load(w2, c->dtype, wb + (int64_t)r * F + f) * g * dyt[r];
-              dh[f] = acc;
-            }
+            /* dh = W2_e^T (g dy): each dh[f] summed over r in ascending order, walking W2 by rows */
+            for (int32_t f = 0; f < F; ++f) dh[f] = 0.0;
+            for (int32_t r = 0; r < d; ++r)
+              for (int32_t f = 0; f < F; ++f) dh[f] += orc_load(w2, c->dtype, wb + (int64_t)r * F + f) * g * dyt[r];
             double* da = sa + slot * F;
             double* db = sb + slot * F;
             for (int32_t f = 0; f < F; ++f) {
@@ -433,13 +465,14 @@ int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* b
               da[f] = dh[f] * bv[f] * s * (1.0 + av[f] * (1.0 - s));
               db[f] = dh[f] * av[f] * s;
             }
-            for (int32_t col = 0; col < d; ++col) {
-              double acc = 0.0;
-              for (int32_t f = 0; f < F; ++f)
-                acc += orc_load(w1, c->dtype, wb + (int64_t)f * d + col) * da[f] +
-                       orc_load(w3, c->dtype, wb + (int64_t)f * d + col) * db[f];
-              dxt[col] += acc;
-            }
+            /* W1_e^T da + W3_e^T db: each column summed over f in ascending order, walking the
+               weights by rows; then added to dx */
+            for (int32_t col = 0; col < d; ++col) o[col] = 0.0;
+            for (int32_t f = 0; f < F; ++f)
+              for (int32_t col = 0; col < d; ++col)
+                o[col] += orc_load(w1, c->dtype, wb + (int64_t)f * d + col) * da[f] +
+                          orc_load(w3, c->dtype, wb + (int64_t)f * d + col) * db[f];
+            for (int32_t col = 0; col < d; ++col) dxt[col] += o[col];
           }
           /* router */
           const double* pt = p + t * E;
@@ -472,15 +505,11 @@ int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* b
     if (failed) rc = ORC_NO_MEM;
   }
   if (!rc) {
-    /* weight gradients, per expert in token order (p now holds dlogit [T,E]) */
+    /* weight gradients (p now holds dlogit [T,E]); every element sums over the tokens of
+       its expert in token order, whichever row of the output a thread takes.
+       Router rows and bias: one expert each. */
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t e = 0; e < E; ++e) {
-      double* g1 = dw1 + (int64_t)e * F * d;
-      double* g3 = dw3 + (int64_t)e * F * d;
-      double* g2 = dw2 + (int64_t)e * d * F;
-      memset(g1, 0, sizeof(double) * (size_t)F * d);
-      memset(g3, 0, sizeof(double) * (size_t)F * d);
-      memset(g2, 0, sizeof(double) * (size_t)d * F);
       double* gr = dwr + (int64_t)e * d;
       memset(gr, 0, sizeof(double) * (size_t)d);
       dbias[e] = 0.0;
@@ -488,22 +517,37 @@ int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* b
         const double dl = p[t * E + e];
         for (int32_t col = 0; col < d; ++col) gr[col] += dl * orc_load(x, c->dtype, t * d + col);
         dbias[e] += dl;
-        for (int32_t j = 0; j < k; ++j) {
-          const int64_t slot = t * k + j;
-          if (idx[slot] != e) continue;
-          const double* da = sa + slot * F;
-          const double* db = sb + slot * F;
-          const double* h = sh + slot * F;
-          const double g = gate[slot];
-          for (int32_t f = 0; f < F; ++f)
-            for (int32_t col = 0; col < d; ++col) {
-              const double xv = orc_load(x, c->dtype, t * d + col);
-              g1[(int64_t)f * d + col] += da[f] * xv;
-              g3[(int64_t)f * d + col] += db[f] * xv;
-            }
-          for (int32_t r = 0; r < d; ++r)
-            for (int32_t f = 0; f < F; ++f) g2[(int64_t)r * F + f] += g * dy[t * d + r] * h[f];
+      }
+    }
+    /* expert weights: dW1 / dW3 row (e, f) and dW2 row (e, r) over the slots routed to e,
+       taken from the dispatch order (ascending token, i.e. the same order as a walk over t) */
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t q = 0; q < (int64_t)E * F; ++q) {
+      const int32_t e = (int32_t)(q / F), f = (int32_t)(q % F);
+      double* g1 = dw1 + q * d;
+      double* g3 = dw3 + q * d;
+      memset(g1, 0, sizeof(double) * (size_t)d);
+      memset(g3, 0, sizeof(double) * (size_t)d);
+      for (int32_t i = offsets[e]; i < offsets[e + 1]; ++i) {
+        const int64_t slot = perm[i], t = slot / k;
+        const double da = sa[slot * F + f], db = sb[slot * F + f];
+        for (int32_t col = 0; col < d; ++col) {
+          const double xv = orc_load(x, c->dtype, t * d + col);
+          g1[col] += da * xv;
+          g3[col] += db * xv;
         }
+      }
+    }
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t q = 0; q < (int64_t)E * d; ++q) {
+      const int32_t e = (int32_t)(q / d), r = (int32_t)(q % d);
+      double* g2 = dw2 + q * F;
+      memset(g2, 0, sizeof(double) * (size_t)F);
+      for (int32_t i = offsets[e]; i < offsets[e + 1]; ++i) {
+        const int64_t slot = perm[i], t = slot / k;
+        const double* h = sh + slot * F;
+        const double gdy = gate[slot] * dy[t * d + r];
+        for (int32_t f = 0; f < F; ++f) g2[f] += gdy * h[f];
       }
     }
   }
@@ -516,5 +560,6 @@ int orc_backward(const orc_cfg* c, const void* x, const void* wr, const float* b
   free(sb);
   free(sh);
   free(dg);
+  free(perm);
   return rc;
 }

@@ -87,3 +87,39 @@ def test_backward_matches_oracle(dims, alpha, renorm, bias, path):
     counts = np.bincount(oidx.reshape(-1), minlength=E)
     for e in np.where(counts == 0)[0]:
         assert not got["dw1"][e].any() and not got["dw2"][e].any(), "an expert without rows has zero gradients"
+
+
+def test_backward_full_size_coarse_e8():
+    """The coarse-expert workload at full size (T=4096, d=2048, E=8, k=2, F=8192, its own
+    seed-0 inputs, as the training-step benchmark runs it) with the balancing-loss term on.
+    About 1024 routed rows per expert: every expert spans a whole group of eight 128-row
+    m-tiles (the pair kernels' scheduling unit), the weight-gradient GEMMs run K over the
+    expert's rows with a partial last block, dH / dX run K = d and F at full size, and the
+    persistent grids take several waves.  Every element of every gradient is compared."""
+    import time
+    from top_routing_grouped_gb300 import moe
+    from top_routing_grouped_gb300.workloads import SHAPES
+    import parity
+    s = SHAPES["coarse_e8"]
+    inp = make_inputs(s, seed=0)
+    alpha = 0.01
+    plan, ws, dy, got = run_backward(moe, s, inp, alpha)
+    counts = plan.views(ws)["expert_counts"].cpu().numpy()
+    host = inp.numpy_for_oracle()
+    orc = oracle.Oracle(s.T, s.d, s.E, s.k, s.F, tau=s.tau, dtype="bf16")
+    z, _, oidx, _ = orc.router(host["x"], host["wr"], host["bias"])
+    assert parity.clear_tokens(z, s.k).all(), "the workload's routing has a near-tie"
+    np.testing.assert_array_equal(np.sort(plan.views(ws)["topk_idx"].cpu().numpy(), 1), np.sort(oidx, 1))
+    t0 = time.perf_counter()
+    ref = orc.backward(host["x"], host["wr"], host["bias"], host["w1"], host["w3"], host["w2"],
+                       dy.float().numpy().astype(np.float64), alpha)
+    secs = time.perf_counter() - t0
+    names = ["dx", "dwr", "dw1", "dw3", "dw2"]
+    errs = {n: rel_err(got[n], ref[n]) for n in names}
+    nerrs = {n: norm_err(got[n], ref[n]) for n in names}
+    print(f"\n[backward coarse_e8 full size, rows/expert {counts.min()}..{counts.max()}, oracle {secs:.0f} s on "
+          f"{oracle.num_threads()} threads] " + " ".join(f"{n}={errs[n]:.2e}/{nerrs[n]:.2e}" for n in names))
+    assert counts.min() >= 8 * 128 - 128, "every expert should span about a whole group of eight m-tiles"
+    for n in names:
+        assert errs[n] <= TOL, f"{n}: {errs[n]}"
+        assert nerrs[n] <= NORM_TOL, f"{n}: norm-wise {nerrs[n]}"

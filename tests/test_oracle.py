@@ -182,6 +182,15 @@ def pin_expert_rows(lib):
             href = silu(w1[e] @ x[t]) * (w3[e] @ x[t])
             np.testing.assert_allclose(h, href, rtol=1e-12, atol=1e-14)
             np.testing.assert_allclose(out, w2[e] @ href, rtol=1e-11, atol=1e-13)
+    # many rows at once, in an arbitrary order with repeats (the batched form the full-size
+    # parity checks use)
+    tk = np.array([4, 0, 2, 2, 1, 4, 3, 0])
+    ex = np.array([2, 1, 0, 2, 1, 0, 2, 0])
+    hs, outs = o.expert_rows(inp["x"], inp["w1"], inp["w3"], inp["w2"], tk, ex)
+    for i, (t, e) in enumerate(zip(tk, ex)):
+        href = silu(w1[e] @ x[t]) * (w3[e] @ x[t])
+        np.testing.assert_allclose(hs[i], href, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(outs[i], w2[e] @ href, rtol=1e-11, atol=1e-13)
 
 
 def pin_renormalised_gates(lib):
@@ -267,6 +276,8 @@ MUTANTS = {
                       "double f = (double)counts[i] / (double)T;"),
     "softmax_unnormalised": ("for (int32_t e = 0; e < E; ++e) pt[e] /= s;", ""),
     "renorm_ignored": ("for (int32_t j = 0; j < k; ++j) gate[t * k + j] /= chosen;", ""),
+    "rows_token_ignored": ("xr[col] = orc_load(x, c->dtype, t[i] * d + col);",
+                           "xr[col] = orc_load(x, c->dtype, i * d + col);"),
     "renorm_over_all": ("for (int32_t j = 0; j < k; ++j) chosen += gate[t * k + j];",
                         "for (int32_t e = 0; e < E; ++e) chosen += pt[e];"),
 }

@@ -111,7 +111,9 @@ MUTANTS = {
                                   "const double dl = pt[e] * dp[e] / c->tau;"),
     "renorm_grad_uncorrected": ("dp[idx[t * k + j]] += (dg[t * k + j] - gdg) / S;",
                                 "dp[idx[t * k + j]] += dg[t * k + j];"),
-    "w3_grad_uses_da": ("g3[(int64_t)f * d + col] += db[f] * xv;", "g3[(int64_t)f * d + col] += da[f] * xv;"),
+    "w3_grad_uses_da": ("g3[col] += db * xv;", "g3[col] += da * xv;"),
+    "w2_grad_wrong_token": ("const double gdy = gate[slot] * dy[t * d + r];",
+                            "const double gdy = gate[slot] * dy[(slot % T) * d + r];"),
 }
 
 

@@ -1,0 +1,98 @@
+"""The operator-level performance model ("Compute-Optimal Is Not Cluster-Optimal", gist.science
+summary, Methodology item 2: an MoE layer priced per operator -- grouped GEMMs, data
+movement, dispatch latency -- fitted to measurements and judged by its prediction error).
+
+CPU: the fit recovers known latencies and rates from exact synthetic samples; the pair-tile
+count follows its closed forms; the wave efficiency charges a partial last wave.
+GPU: the pair-tile count the model prices equals the count the scan kernel writes for the
+expert GEMMs, on every listed bf16 workload and every granularity-sweep layer.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from top_routing_grouped_gb300 import perf_model as pm
+from top_routing_grouped_gb300.workloads import SHAPES, ORDER, granularity_sweep, make_inputs
+
+
+def test_fit_recovers_known_latency_and_rate():
+    rng = np.random.default_rng(0)
+    truth = {st: (0.002 * (i + 1), 1e-9 * (i + 3)) for i, st in enumerate(pm.STAGES)}
+    samples = []
+    for _ in range(6):
+        f = {st: float(rng.uniform(1e6, 1e9)) for st in pm.STAGES}
+        m = {st: truth[st][0] + truth[st][1] * f[st] for st in pm.STAGES}
+        samples.append((f, m))
+    params = pm.fit(samples)
+    for st in pm.STAGES:
+        L, slope = params[st]
+        assert L == pytest.approx(truth[st][0], rel=1e-6, abs=1e-12)
+        assert slope == pytest.approx(truth[st][1], rel=1e-9)
+    # predictions of a held-out point are then exact, and so its error is zero
+    f = {st: 5e8 for st in pm.STAGES}
+    meas = {st: truth[st][0] + truth[st][1] * 5e8 for st in pm.STAGES}
+    meas["total"] = sum(meas.values())
+    pred = pm.predict(params, f)
+    assert max(pm.mape(pred, meas).values()) < 1e-6
+    # rates: B = 1 / slope in GB/s for movers (slope in ms per byte), R in TFLOP/s for GEMMs
+    r = pm.rates(params)
+    assert r["permute_GBps"] == pytest.approx(1e-6 / truth["permute"][1], rel=1e-9)
+    assert r["gemm1_swiglu_TFLOPs"] == pytest.approx(1e-9 / truth["gemm1_swiglu"][1], rel=1e-9)
+
+
+def test_fit_never_returns_a_negative_latency():
+    x = np.array([1.0, 2.0, 3.0, 4.0]) * 1e8
+    samples = [({st: v for st in pm.STAGES}, {st: 2e-9 * v - 0.05 for st in pm.STAGES}) for v in x]
+    for L, slope in pm.fit(samples).values():
+        assert L == 0.0
+        assert slope == pytest.approx(float((x @ (2e-9 * x - 0.05)) / (x @ x)), rel=1e-12)
+
+
+@pytest.mark.parametrize("counts, pairs", [
+    ([0], 0), ([1], 1), ([128], 1), ([129], 1), ([256], 1), ([257], 2),
+    ([1024], 4),               # 8 m-tiles: one whole group of 4 pairs
+    ([1025], 5),               # 9 m-tiles: a whole group, then a group of one m-tile (one pair)
+    ([8 * 128 * 3 + 3 * 128], 14),   # 27 m-tiles: 3 groups of 4 pairs + a group of 3 (2 pairs)
+    ([0, 1, 0, 300, 2048], 1 + 2 + 8),
+])
+def test_pair_tiles_closed_forms(counts, pairs):
+    assert pm.pair_tiles(counts) == pairs
+
+
+def test_features_charge_padding_and_the_last_wave():
+    s = SHAPES["coarse_e8"]
+    counts = [s.N // s.E] * s.E                     # 1024 rows each: 4 pairs, no padding
+    f = pm.features(s, counts)
+    pairs = pm.pair_tiles(counts)
+    t1 = pairs * math.ceil(s.F / pm.GEMM1_TILE_N)   # 32 * 64 = 2048 tiles on 76 slots
+    eff = t1 / (76 * math.ceil(t1 / 76))
+    assert f["gemm1_swiglu"] == pytest.approx(4.0 * pairs * 256 * s.d * s.F / eff)
+    assert f["gemm1_swiglu"] >= 4.0 * s.N * s.d * s.F
+    assert f["route"] == s.T * s.d * 2 + s.N * 8
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [SHAPES[n] for n in ORDER[1:]] + granularity_sweep(), ids=lambda s: s.name)
+def test_pair_tiles_match_the_scan_kernel(shape):
+    """Route and scan only (the stages that build the tile table) on the workload's own
+    inputs; the model's pair count for the routed counts equals the kernel's."""
+    import torch
+    from top_routing_grouped_gb300 import moe
+    inp = make_inputs(shape, seed=0, parts=("x", "wr"))
+    x = inp.x.to("cuda")
+    wr = inp.w_router.to("cuda")
+    bias = None if inp.bias is None else inp.bias.to("cuda")
+    plan = moe.MoEPlan.for_shape(shape)
+    ws = plan.new_workspace()
+    # stages 0-1 read x, W_r and the bias only; the other pointers must merely be valid
+    for stage in (0, 1):
+        plan.forward_stage(stage, x, wr, bias, x, x, x, x, ws)
+    assert plan.device_status(ws) == moe.MOE_OK
+    v = plan.views(ws)
+    counts = v["expert_counts"].cpu().numpy()
+    hdr = v["status"].cpu().numpy()
+    assert counts.sum() == shape.N
+    assert pm.pair_tiles(counts) == int(hdr[4]), (pm.pair_tiles(counts), int(hdr[4]))
+    del ws
+    torch.cuda.empty_cache()

@@ -220,7 +220,7 @@ class MoEPlan:
 
         i32, f32, act = torch.int32, torch.float32, self.act_dtype
         return dict(
-            status=view(v.status, i32, (4,)), aux=view(v.aux, f32, (1,)),
+            status=view(v.status, i32, (8,)), aux=view(v.aux, f32, (1,)),
             topk_idx=view(v.topk_idx, i32, (self.T, self.k)), topk_gate=view(v.topk_gate, f32, (self.T, self.k)),
             expert_counts=view(v.expert_counts, i32, (self.E,)),
             expert_offsets=view(v.expert_offsets, i32, (self.E + 1,)),

@@ -2,7 +2,7 @@
 
 Workload (default): the large layer, T=32768 tokens, d_model=4096, E=64 experts, top-4,
 d_expert=2048, router temperature 0.5, bf16 inputs, seeded synthetic data (the largest of the
-listed layers; --workload picks another).  A step is one whole forward (router, scan, permute,
+listed layers; --workload picks another).  A step is one whole forward (router with its scan, permute,
 grouped SwiGLU GEMM, grouped down-projection with gate and un-permute, combine, balancing
 scalar) through the C ABI.
 
@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE fwd tokens/s and grouped-GEMM TFLOP/s (% of GB300 BF16 peak), 1 GPU"
-STAGES = ["route", "scan", "permute", "gemm1_swiglu", "gemm2_gate", "combine"]
+STAGES = ["route", "permute", "gemm1_swiglu", "gemm2_gate", "combine"]
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
 
@@ -573,7 +573,7 @@ def main():
     if rank == 0:
         pk = peaks()
         gemm_flops = shape.expert_flops
-        g1_ms, g2_ms = stage_ms[3], stage_ms[4]
+        g1_ms, g2_ms = stage_ms[STAGES.index("gemm1_swiglu")], stage_ms[STAGES.index("gemm2_gate")]
         g1_flops = 4 * shape.N * shape.d * shape.F  # the dominant kernel: SwiGLU GEMM (W1 and W3)
         g1_tflops = g1_flops / (g1_ms / 1e3) / 1e12
         gemm_tflops = gemm_flops / ((g1_ms + g2_ms) / 1e3) / 1e12
@@ -581,6 +581,8 @@ def main():
         x_bytes = shape.T * shape.d * 2
         perm_bytes = x_bytes + shape.N * shape.d * 2 + 16 * shape.N
         comb_bytes = shape.N * shape.d * 2 + shape.T * shape.d * 2
+        route_bytes = x_bytes + 8 * shape.N  # x once, the indices and gates out (the scan's tables are small)
+        chained = chained_ms
         line = {
             "metric": METRIC,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -591,10 +593,13 @@ def main():
             "grouped_gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16"],
             "stage_ms": dict(zip(STAGES, stage_ms)),  # from timed region 2
             "stage_ms_back_to_back": dict(zip(STAGES, chained_ms)),  # timed region 3
-            "mover_gbs": {"permute": perm_bytes / (chained_ms[2] / 1e3) / 1e9,
-                          "combine": comb_bytes / (chained_ms[5] / 1e3) / 1e9,
-                          "frac_of_measured_hbm": {"permute": perm_bytes / (chained_ms[2] / 1e3) / 1e9 / pk["hbm"],
-                                                   "combine": comb_bytes / (chained_ms[5] / 1e3) / 1e9 / pk["hbm"]},
+            "mover_gbs": {"permute": perm_bytes / (chained[STAGES.index("permute")] / 1e3) / 1e9,
+                          "combine": comb_bytes / (chained[STAGES.index("combine")] / 1e3) / 1e9,
+                          "route": route_bytes / (chained[0] / 1e3) / 1e9,
+                          "frac_of_measured_hbm": {
+                              "permute": perm_bytes / (chained[STAGES.index("permute")] / 1e3) / 1e9 / pk["hbm"],
+                              "combine": comb_bytes / (chained[STAGES.index("combine")] / 1e3) / 1e9 / pk["hbm"],
+                              "route": route_bytes / (chained[0] / 1e3) / 1e9 / pk["hbm"]},
                           "from": "bytes / per-launch time of 20 back-to-back launches (timed region 3)"},
             "roofline": {"kernel": "gemm1_swiglu", "bound": "tensor", "achieved": g1_tflops, "peak": pk["bf16"],
                          "unit": "TFLOP/s", "frac": g1_tflops / pk["bf16"], "traffic": traffic,

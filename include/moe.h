@@ -106,6 +106,8 @@ typedef struct {
   void* xp;                /* [N,d] act dtype: x rows in dispatch order */
   void* h;                 /* [N,F] act dtype: SwiGLU hidden rows */
   void* yp;                /* [N,d] act dtype: row p = gate * expert output of row p (expert order) */
+  float* expert_psum;      /* [E] sum over the layer's tokens of the softmax p[t,e] (the numerator of
+                              the mean P_e of the balancing scalar) */
 } moe_views;
 
 /* Build a plan for one layer shape (host only; no device work).  Validates the config
@@ -124,7 +126,10 @@ moe_status moe_forward(moe_plan_t plan, const void* x, const void* w_router, con
                        const void* w1, const void* w3, const void* w2, void* y, void* workspace,
                        size_t workspace_bytes, void* stream);
 
-/* Number of kernel stages moe_forward enqueues, and their names. */
+/* Number of kernel stages moe_forward enqueues, and their names: "route" (router, top-k,
+ * per-block counts; its last CTA also runs the scan: per-expert counts, offsets, dispatch
+ * bases, tile table, balancing scalar), "permute", "gemm1_swiglu", "gemm2_gate", "combine".
+ * An expert-stage plan has none. */
 int32_t moe_stage_count(moe_plan_t plan);
 const char* moe_stage_name(moe_plan_t plan, int32_t stage);
 
@@ -180,6 +185,63 @@ moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* view
  * kernel of the last forward recorded (MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL), or MOE_ERR_CUDA
  * if the synchronisation itself failed.  Each moe_forward clears the word first. */
 moe_status moe_get_device_status(moe_plan_t plan, const void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Expert parallelism (§4 Expert Parallelism: experts spread over GPUs; Dispatch sends every
+ * routed row to the GPU that holds its expert, Combine sends the outputs back).
+ *
+ * W ranks; rank r holds its own tokens, the whole router, and the weights of E_l = E / W
+ * experts, r*E_l .. (r+1)*E_l - 1.  A step on rank r, with the exchanges done by the caller's
+ * collectives (the library moves no data between GPUs):
+ *   1. moe_forward_stage "route" and "permute" with a moe_plan over all E experts: the rank's
+ *      rows Xp in expert order -- which is destination-rank order -- with expert_counts and
+ *      gate_perm (moe_workspace_views);
+ *   2. all-to-all of expert_counts viewed [W, E_l]: rank r receives seg_counts [W, E_l];
+ *   3. all-to-all of the rows of Xp and of gate_perm, rank-major as they lie: the received
+ *      rows form W*E_l segments, source-major (segment s: the rows source s/E_l sent to local
+ *      expert s%E_l);
+ *   4. moe_expert_forward over the received rows, in place: gate * E_e(row) in the same order;
+ *   5. the reverse all-to-all of those rows into the rank's Yp (moe_workspace_views);
+ *   6. moe_forward_stage "combine";
+ *   7. optionally the balancing scalar over all ranks: all-reduce of expert_counts and
+ *      expert_psum, then moe_aux_from_totals with the total token count.
+ * ------------------------------------------------------------------------------------- */
+
+typedef struct {
+  int64_t max_rows;        /* R: capacity of the received-row buffers, >= 1 (dropless: at most
+                              W * T_local * min(k, E_l) rows can arrive) */
+  int32_t d_model;         /* d */
+  int32_t n_local_experts; /* E_l: the experts whose weights this rank holds, >= 1 */
+  int32_t n_sources;       /* W: ranks the rows come from; W * E_l <= 256 */
+  int32_t d_expert;        /* F */
+  int32_t act_dtype;       /* moe_dtype of the rows, the weights and the output rows */
+  int32_t path;            /* moe_path */
+  int64_t wait_timeout_ns; /* bound on any device-side wait; <= 0 selects 2 s */
+} moe_expert_config;
+
+/* Plan of the expert stage (host only).  Validates as moe_plan does and returns the workspace
+ * size (status header, per-segment table, tile descriptors, the hidden rows H [R, F]). */
+moe_status moe_expert_plan(const moe_expert_config* cfg, moe_plan_t* plan, size_t* workspace_bytes);
+
+/* The local experts on received rows:  y_rows[p] = gates[p] * E_e(x_rows[p]),
+ *   E_e(v) = W2_e (SiLU(W1_e v) * (W3_e v)),  e = the local expert of p's segment.
+ *   seg_counts [W*E_l] int32 (device): rows per segment, source-major; the rows of segment s
+ *     are x_rows[off_s .. off_s + seg_counts[s]), off_s the sum of the earlier counts.  A
+ *     negative count or a sum above max_rows is recorded as MOE_ERR_INTERNAL
+ *     (moe_get_device_status) and no row is computed.
+ *   x_rows [R,d], gates [R] fp32, y_rows [R,d]: device buffers of max_rows rows; rows past the
+ *     sum of the counts are not written.  w1, w3 [E_l,F,d], w2 [E_l,d,F]: the local experts.
+ * Asynchronous on `stream`; device-side waits are bounded as for moe_forward. */
+moe_status moe_expert_forward(moe_plan_t plan, const int32_t* seg_counts, const void* x_rows, const float* gates,
+                              const void* w1, const void* w3, const void* w2, void* y_rows, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* The balancing scalar from per-expert totals (§3 Load-Balancing Loss):
+ *   aux = E * sum_e (counts[e] / (n_tokens k)) * (psum[e] / n_tokens)
+ * counts [E] int32 and psum [E] fp32 on the device (e.g. expert_counts and expert_psum summed
+ * over ranks), aux_out one fp32 on the device.  Asynchronous on `stream`. */
+moe_status moe_aux_from_totals(int32_t n_experts, int32_t top_k, int64_t n_tokens, const int32_t* counts,
+                               const float* psum, float* aux_out, void* stream);
 
 /* Size in bytes of the static device buffer moe_route_noalloc() works in. */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)

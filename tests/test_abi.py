@@ -51,7 +51,7 @@ def test_plan_workspace_and_stages(moe):
     N = 4096 * 2
     # the workspace holds at least Xp, H and Yslot
     assert p.workspace_bytes >= N * 2048 * 2 * 2 + N * 8192 * 2
-    assert p.stage_names == ["route", "scan", "permute", "gemm1_swiglu", "gemm2_gate", "combine"]
+    assert p.stage_names == ["route", "permute", "gemm1_swiglu", "gemm2_gate", "combine"]
     p2 = moe.MoEPlan(4096, 2048, 8, 2, 8192, dtype="bf16", keep_logits=True)
     assert p2.workspace_bytes >= p.workspace_bytes + 4096 * 8 * 4
 

@@ -4,7 +4,7 @@ movement, dispatch latency -- fitted to measurements and judged by its predictio
 
 CPU: the fit recovers known latencies and rates from exact synthetic samples; the pair-tile
 count follows its closed forms; the wave efficiency charges a partial last wave.
-GPU: the pair-tile count the model prices equals the count the scan kernel writes for the
+GPU: the pair-tile count the model prices equals the count the router's scan writes for the
 expert GEMMs, on every listed bf16 workload and every granularity-sweep layer.
 """
 import math
@@ -75,8 +75,8 @@ def test_features_charge_padding_and_the_last_wave():
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape", [SHAPES[n] for n in ORDER[1:]] + granularity_sweep(), ids=lambda s: s.name)
 def test_pair_tiles_match_the_scan_kernel(shape):
-    """Route and scan only (the stages that build the tile table) on the workload's own
-    inputs; the model's pair count for the routed counts equals the kernel's."""
+    """The route stage only (the router, whose last CTA builds the tile table) on the
+    workload's own inputs; the model's pair count for the routed counts equals the kernel's."""
     import torch
     from top_routing_grouped_gb300 import moe
     inp = make_inputs(shape, seed=0, parts=("x", "wr"))
@@ -85,9 +85,8 @@ def test_pair_tiles_match_the_scan_kernel(shape):
     bias = None if inp.bias is None else inp.bias.to("cuda")
     plan = moe.MoEPlan.for_shape(shape)
     ws = plan.new_workspace()
-    # stages 0-1 read x, W_r and the bias only; the other pointers must merely be valid
-    for stage in (0, 1):
-        plan.forward_stage(stage, x, wr, bias, x, x, x, x, ws)
+    # the route stage reads x, W_r and the bias only; the other pointers must merely be valid
+    plan.forward_stage(0, x, wr, bias, x, x, x, x, ws)
     assert plan.device_status(ws) == moe.MOE_OK
     v = plan.views(ws)
     counts = v["expert_counts"].cpu().numpy()

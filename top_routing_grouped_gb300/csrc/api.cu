@@ -22,6 +22,10 @@ struct moe_plan_s {
   int device = -1;  // device the cached attributes belong to
   int num_sms = 0;
   int64_t timeout_ns;
+  // expert-stage plans (moe_expert_plan): rows from n_src sources, n_src * E_l segments
+  bool expert_stage = false;
+  int n_src = 0;
+  int n_seg = 0;
 };
 
 namespace {
@@ -47,8 +51,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr const char* kStageNames[] = {"route", "scan", "permute", "gemm1_swiglu", "gemm2_gate", "combine"};
-constexpr int kNumStages = 6;
+// "route" covers the router, top-k, per-block counts and (in its last CTA) the scan: offsets,
+// dispatch bases, tile descriptors and the balancing scalar.
+constexpr const char* kStageNames[] = {"route", "permute", "gemm1_swiglu", "gemm2_gate", "combine"};
+constexpr int kNumStages = 5;
 
 // Attributes of the current device, cached on the plan.
 moe_status bind_device(moe_plan_t plan) {
@@ -91,6 +97,7 @@ WsLayout ws_layout(const Shape& s) {
   L.topk_gate = take(N * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
+  L.ptot = take(E * 4);
   L.blk_base = take(nb * E * 4);
   L.mt_desc = take((size_t)s.max_groups * moe::kGroupM * 16);
   L.pr_desc = take((size_t)s.max_groups * (moe::kGroupM / 2) * 16);
@@ -137,6 +144,7 @@ Ws ws_bind(const Shape& s, void* base) {
   w.topk_gate = reinterpret_cast<float*>(b + L.topk_gate);
   w.counts = reinterpret_cast<int32_t*>(b + L.counts);
   w.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  w.ptot = reinterpret_cast<float*>(b + L.ptot);
   w.blk_base = reinterpret_cast<int32_t*>(b + L.blk_base);
   w.mt_desc = reinterpret_cast<int4*>(b + L.mt_desc);
   w.pr_desc = reinterpret_cast<int4*>(b + L.pr_desc);
@@ -169,6 +177,28 @@ Ws ws_bind(const Shape& s, void* base) {
 }
 
 const Shape* plan_shape(moe_plan_t plan) { return &plan->shape; }
+bool plan_is_layer(moe_plan_t plan) { return plan && !plan->expert_stage; }
+
+// Workspace of an expert-stage plan: status header, per-segment counts and offsets, the tile
+// descriptors and the SwiGLU hidden rows H [N, F]; the received rows, their gates and the
+// output rows are the caller's buffers.
+WsLayout expert_layout(const Shape& s, int n_seg) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  L.hdr = take(64 * sizeof(uint32_t));
+  L.counts = take((size_t)n_seg * 4);
+  L.offsets = take(((size_t)n_seg + 1) * 4);
+  L.mt_desc = take((size_t)s.max_groups * moe::kGroupM * 16);
+  L.pr_desc = take((size_t)s.max_groups * (moe::kGroupM / 2) * 16);
+  L.h = take((size_t)s.N * (size_t)s.F * (s.act_bf16 ? 2 : 4));
+  L.total = off;
+  return L;
+}
 
 moe_status set_last_error(moe_status st, const char* msg) {
   g_last_error = msg;
@@ -259,10 +289,10 @@ moe_status moe_plan(const moe_config* cfg, moe_plan_t* plan, size_t* workspace_b
 
 void moe_plan_destroy(moe_plan_t plan) { delete plan; }
 
-int32_t moe_stage_count(moe_plan_t plan) { return plan ? kNumStages : 0; }
+int32_t moe_stage_count(moe_plan_t plan) { return plan && !plan->expert_stage ? kNumStages : 0; }
 
 const char* moe_stage_name(moe_plan_t plan, int32_t stage) {
-  if (!plan || stage < 0 || stage >= kNumStages) return nullptr;
+  if (!plan || plan->expert_stage || stage < 0 || stage >= kNumStages) return nullptr;
   return kStageNames[stage];
 }
 
@@ -270,6 +300,7 @@ static moe_status check_forward_args(moe_plan_t plan, const void* x, const void*
                                      const void* w1, const void* w3, const void* w2, void* y, void* workspace,
                                      size_t workspace_bytes) {
   if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+  if (plan->expert_stage) return fail(MOE_ERR_INVALID_ARG, "an expert-stage plan runs only moe_expert_forward");
   const void* ptrs[] = {x, w_router, w1, w3, w2, y};
   const char* names[] = {"x", "w_router", "w1", "w3", "w2", "y"};
   for (int i = 0; i < 6; ++i) {
@@ -292,16 +323,16 @@ static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& 
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0:
-      e = cudaMemsetAsync(ws.hdr, 0, 4 * sizeof(uint32_t), st);
+      // the status word and the router's completion ticket start at zero
+      e = cudaMemsetAsync(ws.hdr, 0, moe::kHdrClearWords * sizeof(uint32_t), st);
       if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
       e = plan->tc ? moe::launch_route_tc(s, ws, w, plan->num_sms, plan->timeout_ns, st)
                    : moe::launch_route_simt(s, ws, w, st);
       break;
-    case 1: e = moe::launch_scan(s, ws, pdl, st); break;
-    case 2: e = moe::launch_permute(s, ws, w, plan->num_sms, pdl, st); break;
-    case 3:
-    case 4: {
-      const int mode = stage == 3 ? 1 : 2;
+    case 1: e = moe::launch_permute(s, ws, w, plan->num_sms, pdl, st); break;
+    case 2:
+    case 3: {
+      const int mode = stage == 2 ? 1 : 2;
       const bool stall = mode == 1 && (plan->cfg.flags & MOE_FLAG_TEST_STALL) != 0;
       if (plan->pair)
         e = moe::launch_gemm_tc_pair(mode, s, ws, w, plan->num_sms, plan->timeout_ns, stall, pdl, st);
@@ -312,7 +343,7 @@ static moe_status run_stage(moe_plan_t plan, int32_t stage, const moe::Weights& 
                       : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, pdl, st);
       break;
     }
-    case 5: e = moe::launch_combine(s, ws, w, plan->num_sms, pdl, st); break;
+    case 4: e = moe::launch_combine(s, ws, w, plan->num_sms, pdl, st); break;
     default: return fail(MOE_ERR_INVALID_ARG, "stage %d out of range", stage);
   }
   if (e != cudaSuccess) {
@@ -443,6 +474,7 @@ moe_status moe_backward(moe_plan_t plan, const void* x, const void* w_router, co
 
 moe_status moe_aux_loss(moe_plan_t plan, const void* workspace, float* aux_out, void* stream) {
   if (!plan || !workspace || !aux_out) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  if (plan->expert_stage) return fail(MOE_ERR_INVALID_ARG, "an expert-stage plan has no balancing scalar");
   if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const char* src = static_cast<const char*>(workspace) + plan->layout.aux;
   cudaError_t e = cudaMemcpyAsync(aux_out, src, sizeof(float), cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
@@ -452,6 +484,7 @@ moe_status moe_aux_loss(moe_plan_t plan, const void* workspace, float* aux_out, 
 
 moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* v) {
   if (!plan || !workspace || !v) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  if (plan->expert_stage) return fail(MOE_ERR_INVALID_ARG, "an expert-stage plan's workspace has no views");
   const moe::Ws w = moe::ws_bind(plan->shape, workspace);
   v->status = w.hdr + moe::kHdrStatus;
   v->aux = w.aux;
@@ -467,6 +500,120 @@ moe_status moe_workspace_views(moe_plan_t plan, void* workspace, moe_views* v) {
   v->xp = w.xp;
   v->h = w.h;
   v->yp = w.yp;
+  v->expert_psum = w.ptot;
+  return MOE_OK;
+}
+
+moe_status moe_expert_plan(const moe_expert_config* cfg, moe_plan_t* plan, size_t* workspace_bytes) {
+  if (!cfg || !plan || !workspace_bytes) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  *plan = nullptr;
+  const moe_expert_config& c = *cfg;
+  if (c.max_rows < 1 || c.d_model < 1 || c.d_expert < 1 || c.n_local_experts < 1 || c.n_sources < 1)
+    return fail(MOE_ERR_INVALID_ARG, "max_rows, d_model, d_expert, n_local_experts, n_sources must be >= 1");
+  if ((int64_t)c.n_local_experts * c.n_sources > moe::kMaxExperts)
+    return fail(MOE_ERR_INVALID_ARG, "n_sources * n_local_experts must be <= %d", moe::kMaxExperts);
+  if (c.act_dtype != MOE_F32 && c.act_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "bad act_dtype");
+  if (c.path != MOE_PATH_AUTO && c.path != MOE_PATH_SIMT && c.path != MOE_PATH_TC_1SM)
+    return fail(MOE_ERR_INVALID_ARG, "bad path");
+  if (c.max_rows > (int64_t)INT32_MAX / 2 ||
+      c.max_rows * (int64_t)(c.d_model > c.d_expert ? c.d_model : c.d_expert) > ((int64_t)1 << 40))
+    return fail(MOE_ERR_UNSUPPORTED, "max_rows (or the rows' activations) too large");
+  const bool bf16 = c.act_dtype == MOE_BF16;
+  if (c.path == MOE_PATH_TC_1SM && !bf16) return fail(MOE_ERR_INVALID_ARG, "MOE_PATH_TC_1SM needs bf16 inputs");
+  const bool tc = bf16 && c.path != MOE_PATH_SIMT && moe::kTensorCorePathBuilt;
+  if (!bf16 && c.d_model % 4 != 0) return fail(MOE_ERR_UNSUPPORTED, "fp32 layers need d_model %% 4 == 0");
+  if (bf16 && c.d_model % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "bf16 layers need d_model %% 8 == 0");
+  if (tc && (c.d_model % 64 != 0 || c.d_expert % 64 != 0))
+    return fail(MOE_ERR_UNSUPPORTED, "the tensor-core path needs d_model and d_expert multiples of 64 (use MOE_PATH_SIMT)");
+  moe_plan_s* p = new (std::nothrow) moe_plan_s();
+  if (!p) return fail(MOE_ERR_INTERNAL, "out of host memory");
+  p->cfg = moe_config{};
+  p->cfg.path = c.path;
+  moe::Shape& s = p->shape;
+  s.T = c.max_rows;
+  s.N = c.max_rows;
+  s.d = c.d_model;
+  s.E = c.n_local_experts;  // weight experts: the GEMMs' weight tensors hold E_l experts
+  s.k = 1;
+  s.F = c.d_expert;
+  s.nblk = 0;
+  s.tau = 1.f;
+  s.act_bf16 = bf16 ? 1 : 0;
+  s.out_bf16 = s.act_bf16;
+  p->n_src = c.n_sources;
+  p->n_seg = c.n_sources * c.n_local_experts;
+  // groups of up to kGroupM m-tiles per segment (as moe_plan bounds them per expert)
+  s.max_groups = (int)(c.max_rows / ((int64_t)moe::kTileM * moe::kGroupM) + 2 * (int64_t)p->n_seg + 2);
+  p->layout = moe::expert_layout(s, p->n_seg);
+  p->tc = tc;
+  p->pair = tc && c.path == MOE_PATH_AUTO;
+  p->timeout_ns = c.wait_timeout_ns > 0 ? c.wait_timeout_ns : 2000000000LL;
+  p->expert_stage = true;
+  *plan = p;
+  *workspace_bytes = p->layout.total;
+  g_last_error.clear();
+  return MOE_OK;
+}
+
+moe_status moe_expert_forward(moe_plan_t plan, const int32_t* seg_counts, const void* x_rows, const float* gates,
+                              const void* w1, const void* w3, const void* w2, void* y_rows, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+  if (!plan->expert_stage) return fail(MOE_ERR_INVALID_ARG, "moe_expert_forward needs a plan made by moe_expert_plan");
+  const void* ptrs[] = {seg_counts, x_rows, gates, w1, w3, w2, y_rows};
+  const char* names[] = {"seg_counts", "x_rows", "gates", "w1", "w3", "w2", "y_rows"};
+  for (int i = 0; i < 7; ++i) {
+    if (!ptrs[i]) return fail(MOE_ERR_INVALID_ARG, "%s is null", names[i]);
+    if (!aligned(ptrs[i], 16)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  if (!workspace || !aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan->layout.total)
+    return fail(MOE_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, plan->layout.total);
+  moe_status st = bind_device(plan);
+  if (st != MOE_OK) return st;
+  const moe::Shape& s = plan->shape;
+  const moe::WsLayout& L = plan->layout;
+  char* b = static_cast<char*>(workspace);
+  moe::Ws ws{};
+  ws.hdr = reinterpret_cast<uint32_t*>(b + L.hdr);
+  ws.counts = reinterpret_cast<int32_t*>(b + L.counts);
+  ws.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  ws.mt_desc = reinterpret_cast<int4*>(b + L.mt_desc);
+  ws.pr_desc = reinterpret_cast<int4*>(b + L.pr_desc);
+  ws.h = b + L.h;
+  ws.xp = const_cast<void*>(x_rows);
+  ws.yp = y_rows;
+  ws.gate_perm = const_cast<float*>(gates);
+  const moe::Weights w{nullptr, nullptr, nullptr, w1, w3, w2, nullptr};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws.hdr, 0, moe::kHdrClearWords * sizeof(uint32_t), cs);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  if ((e = moe::launch_seg_scan(s, ws, seg_counts, plan->n_seg, s.E, cs)) != cudaSuccess)
+    return cuda_fail(e, "launching the segment scan");
+  for (int mode = 1; mode <= 2; ++mode) {
+    if (plan->pair)
+      e = moe::launch_gemm_tc_pair(mode, s, ws, w, plan->num_sms, plan->timeout_ns, false, true, cs);
+    else if (plan->tc)
+      e = moe::launch_gemm_tc(mode, s, ws, w, plan->num_sms, plan->timeout_ns, false, true, cs);
+    else
+      e = mode == 1 ? moe::launch_gemm1_simt(s, ws, w, plan->num_sms, true, cs)
+                    : moe::launch_gemm2_simt(s, ws, w, plan->num_sms, true, cs);
+    if (e != cudaSuccess) return cuda_fail(e, mode == 1 ? "launching the SwiGLU GEMM" : "launching the down-projection");
+  }
+  return MOE_OK;
+}
+
+moe_status moe_aux_from_totals(int32_t n_experts, int32_t top_k, int64_t n_tokens, const int32_t* counts,
+                               const float* psum, float* aux_out, void* stream) {
+  if (n_experts < 1 || n_experts > moe::kMaxExperts || top_k < 1 || top_k > n_experts || n_tokens < 1)
+    return fail(MOE_ERR_INVALID_ARG, "need 1 <= n_experts <= %d, 1 <= top_k <= n_experts, n_tokens >= 1",
+                moe::kMaxExperts);
+  if (!counts || !psum || !aux_out) return fail(MOE_ERR_INVALID_ARG, "null argument");
+  if (!aligned(counts, 16) || !aligned(psum, 16) || !aligned(aux_out, 4))
+    return fail(MOE_ERR_INVALID_ARG, "counts and psum must be 16-byte aligned");
+  cudaError_t e = moe::launch_aux_totals(n_experts, top_k, n_tokens, counts, psum, aux_out,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the balancing scalar");
   return MOE_OK;
 }
 

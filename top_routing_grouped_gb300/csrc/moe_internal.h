@@ -14,7 +14,10 @@ constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 256;
 
 // Status word slots in the workspace header.
-enum : int { kHdrStatus = 0, kHdrWhere = 1, kHdrNumGroups = 2, kHdrNumMTiles = 3, kHdrNumPairs = 4 };
+// kHdrTicket counts the router CTAs that have finished (the last one runs the scan); the
+// words up to kHdrClearWords are cleared before every forward.
+enum : int { kHdrStatus = 0, kHdrWhere = 1, kHdrNumGroups = 2, kHdrNumMTiles = 3, kHdrNumPairs = 4, kHdrTicket = 5,
+             kHdrClearWords = 8 };
 
 // Layer shape as the kernels see it.
 struct Shape {
@@ -43,6 +46,7 @@ struct Ws {
   float* topk_gate;     // [N]
   int32_t* counts;      // [E]
   int32_t* offsets;     // [E+1]
+  float* ptot;          // [E] sum over the tokens of p[t,e] (the router's scan; null where unused)
   int32_t* blk_base;    // [nblk, E] first row of (block, expert) in dispatch order
   // Tile descriptors: entry q describes the scheduling group that owns m-tile q (mt_desc) or
   // m-tile pair q (pr_desc), so that a tile id decodes with one load:
@@ -81,7 +85,7 @@ struct Ws {
 
 // Fixed layout of one workspace: byte offsets of each region.
 struct WsLayout {
-  size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, blk_base,
+  size_t hdr, aux, blk_cnt, blk_psum, local_rank, topk_idx, topk_gate, counts, offsets, ptot, blk_base,
       mt_desc, pr_desc, perm_src, perm_slot, gate_perm, slot_pos, logits, xp, h,
       yp, a1, a3, probs, dyp, dop, dab, dab_tail, dop_tail, dgp, dxslot, dlogit, dl_hi, dl_lo, dwr_part, dwr_part_b, total;
 };
@@ -142,11 +146,16 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 // Kernel launchers (each returns the launch's cudaError_t).  `pdl`: see launch_kernel.
 cudaError_t launch_route_simt(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st);
-cudaError_t launch_scan(const Shape& s, const Ws& ws, bool pdl, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_gemm1_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_gemm2_simt(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const Ws& ws, const Weights& w, int num_sms, bool pdl, cudaStream_t st);
+// expert stage of expert parallelism: the tile table over received segments; the balancing
+// scalar from per-expert totals
+cudaError_t launch_seg_scan(const Shape& s, const Ws& ws, const int32_t* seg_counts, int n_seg, int n_local,
+                            cudaStream_t st);
+cudaError_t launch_aux_totals(int E, int k, int64_t T, const int32_t* counts, const float* psum, float* aux_out,
+                              cudaStream_t st);
 
 cudaError_t launch_gather_dy(const Shape& s, const Ws& ws, const void* dy, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_router_bwd(const Shape& s, const Ws& ws, float alpha, int n_tiles_dh, bool pdl, cudaStream_t st);
@@ -157,8 +166,10 @@ cudaError_t launch_dwr_reduce(const Shape& s, const Ws& ws, float* dwr, float* d
 int dwr_chunks(const Shape& s);
 int dwr_chunk_tokens(const Shape& s);
 
-// Plan internals for entry points defined outside api.cu.
+// Plan internals for entry points defined outside api.cu.  plan_is_layer: a plan made by
+// moe_plan (not an expert-stage plan).
 const Shape* plan_shape(moe_plan_t plan);
+bool plan_is_layer(moe_plan_t plan);
 moe_status set_last_error(moe_status st, const char* msg);
 
 }  // namespace moe

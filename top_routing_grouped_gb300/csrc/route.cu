@@ -1,5 +1,6 @@
 // route.cu -- router: logits, softmax, top-k, gates, per-block histogram, local dispatch
-// ranks and softmax partial sums for the balancing scalar.
+// ranks and softmax partial sums for the balancing scalar; the last CTA to finish also runs
+// the scan (route_scan.cuh).
 //
 // After "Distributed Training Part 4 ... MoE + Expert Parallelism" (jesamkim ai-tech-blog):
 // §3 Structure (router = linear layer + softmax over experts; only the TopK experts are
@@ -11,6 +12,7 @@
 
 #include "device_common.cuh"
 #include "route_common.cuh"
+#include "route_scan.cuh"
 
 namespace moe {
 
@@ -63,12 +65,16 @@ __global__ void __launch_bounds__(kRouteBlock) route_simt_kernel(Shape s, Ws ws,
     z_s[r * ldz + e] = v / s.tau;
   }
   route_finish(s, ws, blk, r, z_s, ldz, mask_s, /*bar_id=*/1);
+  __syncthreads();  // the block's shared tables are no longer needed: the scan may reuse them
+  route_scan_if_last(s, ws, kRouteBlock, s.nblk, smem_raw);
 }
 
 size_t route_simt_smem(const Shape& s) {
-  return sizeof(float) * ((size_t)kRouteBlock * (s.E + 1) + (size_t)kRouteBlock * (kRouteChunk + 1) +
-                          (size_t)s.E * (kRouteChunk + 1)) +
-         sizeof(uint32_t) * (4 * (size_t)s.E + 2 * kRouteBlock);
+  const size_t body = sizeof(float) * ((size_t)kRouteBlock * (s.E + 1) + (size_t)kRouteBlock * (kRouteChunk + 1) +
+                                       (size_t)s.E * (kRouteChunk + 1)) +
+                      sizeof(uint32_t) * (4 * (size_t)s.E + 2 * kRouteBlock);
+  const size_t scan = route_scan_smem(s, kRouteBlock);
+  return body > scan ? body : scan;
 }
 
 cudaError_t launch_route_simt(const Shape& s, const Ws& ws, const Weights& w, cudaStream_t st) {

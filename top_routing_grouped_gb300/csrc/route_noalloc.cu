@@ -163,6 +163,10 @@ extern "C" moe_status moe_route_noalloc(moe_plan_t plan, const void* x, const vo
       snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: every device pointer must be 16-byte aligned");
       return set_last_error(MOE_ERR_INVALID_ARG, g_msg);
     }
+  if (!plan_is_layer(plan)) {
+    snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: needs a plan made by moe_plan");
+    return set_last_error(MOE_ERR_INVALID_ARG, g_msg);
+  }
   Shape s = *plan_shape(plan);
   if (s.has_bias && (!router_bias || reinterpret_cast<uintptr_t>(router_bias) % 16 != 0)) {
     snprintf(g_msg, sizeof g_msg, "moe_route_noalloc: the plan has a router bias: router_bias must be a 16-byte aligned pointer");

@@ -7,11 +7,14 @@
 // layer streams x once (2 bytes per element against 2E flops), so it is bound by HBM, not by
 // the MMA; the tensor cores only keep the E dot products per token off the SIMT pipes.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
-// warps 2..9 epilogue, two per TMEM lane quarter (warp w reads lanes 32*(w%4)..: rows of its
-// 32 tokens), one for each half of the experts; each token is finished by a pair of threads.
+// Warp roles (64 + 128 Q threads, Q = 2 or 4): warp 0 TMA producer, warp 1 TMEM allocator +
+// MMA issuer, warps 2..2+4Q-1 epilogue, Q per TMEM lane quarter (warp w reads lanes
+// 32*(w%4)..: rows of its 32 tokens), one for each of Q contiguous ranges of the experts; each
+// token is finished by Q threads (Q = 4 when E > 64, where the per-token top-k and softmax
+// work would otherwise leave the epilogue latency-bound on too few warps).
 // Waits are bounded as in the expert GEMMs; if one runs out the block still finishes its
 // epilogue on zero logits (valid routing, status MOE_ERR_TIMEOUT) so no barrier is left open.
+// The CTA that finishes its token block last also runs the scan (route_scan.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -19,15 +22,16 @@
 
 #include "gemm_tc.h"
 #include "route_common.cuh"
+#include "route_scan.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kBK = 64;
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;  // warps 2..9
 constexpr int kMaxStages = 8;
+// threads of the kernel with Q epilogue threads per token
+__host__ __device__ constexpr int route_threads(int q) { return 64 + q * kRouteBlock; }
 constexpr int kXBytes = kRouteBlock * kBK * 2;  // 16 KB
 constexpr int kMaxAcc = 4;                       // TMEM accumulators the K loop may use
 
@@ -45,10 +49,11 @@ struct RouteCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int vote[8];
+  int vote[16];
 };
 
 struct RouteGeom {
+  int q;            // epilogue threads per token (2 or 4)
   int split;        // CTAs (one cluster) sharing one token block, each on 1/split of d
   int kb_per;       // 64-column K blocks per CTA
   int recv_bytes;   // leader's buffer for the other CTAs' partial logits
@@ -61,15 +66,20 @@ struct RouteGeom {
   size_t smem;      // dynamic shared memory
 };
 
-// The two threads of a token exchange their top-k values (kMaxTopK floats each), their parts
-// of the softmax denominator and their marked-expert bitmasks (8 words each).
-constexpr int xchg_bytes() { return 2 * kRouteBlock * (kMaxTopK + 1 + 8) * 4; }
+// The Q threads of a token exchange their top-k values (kMaxTopK floats each), their parts
+// of the softmax denominator, their marked-expert bitmasks (8 words each) and their counts of
+// experts equal to the k-th value; the chosen experts of each token's slots follow
+// (kMaxTopK words per token).
+__host__ __device__ constexpr int xchg_bytes(int q) {
+  return q * kRouteBlock * (kMaxTopK + 1 + 8 + 1) * 4 + kRouteBlock * kMaxTopK * 4;
+}
 
-// Experts of half h of the columns: 16-column chunks [0, hc) and [hc, chunks).
-__host__ __device__ inline int expert_half_split(int e_pad) { return 16 * ((e_pad / 16 + 1) / 2); }
+// Columns of range h of Q: whole 16-column chunks, [16 (h nch / Q), 16 ((h+1) nch / Q)).
+__host__ __device__ inline int range_col(int e_pad, int h, int q) { return 16 * ((h * (e_pad / 16)) / q); }
 
 RouteGeom route_geom(const Shape& s, int num_sms) {
   RouteGeom g;
+  g.q = s.E > 64 ? 4 : 2;
   g.e_pad = ((s.E + 15) / 16) * 16;
   if (g.e_pad < 16) g.e_pad = 16;
   const int kblocks = s.d / kBK;
@@ -92,8 +102,13 @@ RouteGeom route_geom(const Shape& s, int num_sms) {
   if (g.stages > g.kb_per) g.stages = g.kb_per;
   if (g.stages < 2) g.stages = 2;
   // logits, then the masks and per-row floats of the finish, then its pair exchange
-  const int zs = kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4 + xchg_bytes();
+  // logits, masks and per-row floats, the exchange, then exp(z - max) per logit for the
+  // softmax sums
+  const int zs = 2 * kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4 + xchg_bytes(g.q);
   g.body_bytes = g.stages * g.stage_bytes > zs ? g.stages * g.stage_bytes : zs;
+  // the scan of the last CTA reuses the body
+  const int scan = (int)route_scan_smem(s, route_threads(g.q));
+  if (g.body_bytes < scan) g.body_bytes = scan;
   g.body_bytes = (g.body_bytes + 1023) / 1024 * 1024;
   // The tensor core's fp32 accumulation chain over K = d loses more than a SIMT sum; K-block
   // kb goes to accumulator kb % n_acc and the epilogue adds the n_acc partial sums in fp32
@@ -120,35 +135,40 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]
       : "memory");
 }
 
-// Called by the 256 epilogue threads once z_s[r * ldz + e] holds the finished logits of the
-// block's token r (ldz odd): thread (r, h) owns the experts [e_lo, e_hi) of half h.  Same
-// results as route_finish (route_common.cuh), with the per-token work split over two threads:
-//   1. each thread keeps the KS largest values of its half (max/min network); the pair swaps
-//      lists through shared memory and each merges the other's into its own, so both hold
-//      the KS largest of the row (the same multiset, in the same descending order);
-//   2. each thread sums exp(z - max) over its half and marks its experts at or above the k-th
-//      value; the half-0 thread adds the two sums (half 0 first) and assigns the slots over
-//      both halves' marks in ascending expert order (ties: lower index first), then writes the
-//      gates, indices and the block's bitmasks;
-//   3. ranks from the bitmasks; per-block counts; per-expert sums of p over the block's rows
-//      by the eight warps (a lane adds rows lane, +32, +64, +96 in that order, then a fixed
-//      butterfly).
-template <int KS>
-__device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo,
+// Called by the Q*128 epilogue threads once z_s[r * ldz + e] holds the finished logits of the
+// block's token r (ldz odd): thread (r, h) owns the experts [e_lo, e_hi) of range h < Q.  Same
+// results as route_finish (route_common.cuh), with the per-token work split over Q threads:
+//   1. each thread keeps the KS largest values of its range (max/min network); the Q threads
+//      of a token swap lists through shared memory and each merges the others' into its own,
+//      so all hold the KS largest of the row (the same multiset, in the same descending order);
+//   2. each thread sums q = exp(z - max) over its range (keeping q for step 3), marks its
+//      experts at or above the k-th value and counts those equal to it; every thread of the
+//      token then adds the Q sums (range order).  When the k largest values are distinct and
+//      only one expert holds the k-th (the common case), slot j holds the expert whose value is
+//      the j-th largest, so each thread places its own marked experts (slot = number of larger
+//      values) and writes their gates, indices and bitmask bits; otherwise the range-0 thread
+//      assigns every slot over all ranges' marks in ascending expert order (ties: lower index
+//      first) -- the rule itself, of which the common case is a shortcut;
+//   3. ranks from the bitmasks (the token's slots split over its Q threads); per-block counts;
+//      per-expert sums of p = q / sum over the block's rows by the 4Q warps (a lane adds rows
+//      lane, +32, +64, +96 in that order, then a fixed butterfly).
+template <int KS, int Q>
+__device__ __forceinline__ void route_finishq_k(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo,
                                                 int e_hi, float* z_s, int ldz, uint32_t* mask_s, int bar_id) {
+  constexpr int NT = Q * kRouteBlock;
   const int E = s.E, k = s.k;
   const int tid = h * kRouteBlock + r;
   const int64_t t = (int64_t)blk * kRouteBlock + r;
   const bool valid = t < s.T;
   float* m_s = reinterpret_cast<float*>(mask_s + 4 * E);
   float* inv_s = m_s + kRouteBlock;
-  float* xbv = inv_s + kRouteBlock;                                         // [2][128][kMaxTopK]
-  float* xsum = xbv + 2 * kRouteBlock * kMaxTopK;                           // [2][128]
-  uint32_t* xtake = reinterpret_cast<uint32_t*>(xsum + 2 * kRouteBlock);   // [2][128][8]
-  for (int i = tid; i < 4 * E; i += kEpiThreads) mask_s[i] = 0u;
+  float* xbv = inv_s + kRouteBlock;                                         // [Q][128][kMaxTopK]
+  float* xsum = xbv + Q * kRouteBlock * kMaxTopK;                           // [Q][128]
+  uint32_t* xtake = reinterpret_cast<uint32_t*>(xsum + Q * kRouteBlock);   // [Q][128][8]
+  for (int i = tid; i < 4 * E; i += NT) mask_s[i] = 0u;
   const uint32_t zr = static_cast<uint32_t>(__cvta_generic_to_shared(z_s + r * ldz));
 
-  // pass 1: the KS largest values of this half (fmaxf(z, -inf) ranks a NaN as -inf)
+  // pass 1: the KS largest values of this range (fmaxf(z, -inf) ranks a NaN as -inf)
   float bv[KS];
 #pragma unroll
   for (int j = 0; j < KS; ++j) bv[j] = -INFINITY;
@@ -171,14 +191,18 @@ __device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, in
   }
 #pragma unroll
   for (int j = 0; j < KS; ++j) xbv[tid * kMaxTopK + j] = bv[j];
-  named_barrier(bar_id, kEpiThreads);
-  // merge the other half's list into this one
+  named_barrier(bar_id, NT);
+  // merge the other ranges' lists into this one
 #pragma unroll
-  for (int i = 0; i < KS; ++i) {
-    const float v = xbv[((1 - h) * kRouteBlock + r) * kMaxTopK + i];
+  for (int o = 1; o < Q; ++o) {
+    const int hh = (h + o) % Q;
 #pragma unroll
-    for (int j = KS - 1; j > 0; --j) bv[j] = fmaxf(bv[j], fminf(v, bv[j - 1]));
-    bv[0] = fmaxf(bv[0], v);
+    for (int i = 0; i < KS; ++i) {
+      const float v = xbv[(hh * kRouteBlock + r) * kMaxTopK + i];
+#pragma unroll
+      for (int j = KS - 1; j > 0; --j) bv[j] = fmaxf(bv[j], fminf(v, bv[j - 1]));
+      bv[0] = fmaxf(bv[0], v);
+    }
   }
   if (nan_seen) record_error(ws, MOE_ERR_INTERNAL, 0x100u);
   const float m = bv[0];
@@ -190,11 +214,17 @@ __device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, in
 #pragma unroll
   for (int j = 0; j < KS; ++j) eq_left -= (j < k && bv[j] > thr) ? 1 : 0;
 
-  // pass 2: this half's part of the softmax denominator and its marked experts
+  // pass 2: this range's part of the softmax denominator (q = exp(z - max) kept in qs), its
+  // marked experts and its count of experts equal to the k-th value
+  int* xcnt = reinterpret_cast<int*>(xtake + Q * kRouteBlock * 8);  // [Q][128]
+  int* slotv = xcnt + Q * kRouteBlock;                               // [128][kMaxTopK]
+  float* qs = reinterpret_cast<float*>(slotv + kRouteBlock * kMaxTopK);  // [128][ldz]
+  const uint32_t qr = static_cast<uint32_t>(__cvta_generic_to_shared(qs + r * ldz));
   uint32_t* my_take = xtake + tid * 8;
 #pragma unroll
   for (int w = 0; w < 8; ++w) my_take[w] = 0u;
   float sum_h = 0.f;
+  int n_thr = 0;
   if (valid) {
     uint32_t cur = 0u;
     int cw = e_lo >> 5;
@@ -212,27 +242,68 @@ __device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, in
           cur = 0u;
           cw = e >> 5;
         }
-        sum_h += expf(v4[u] - m);
+        const float q = expf(v4[u] - m);
+        st_shared_f32(qr + 4u * (uint32_t)e, q);
+        sum_h += q;
         cur |= (v4[u] >= thr ? 1u : 0u) << (e & 31);
+        n_thr += v4[u] == thr ? 1 : 0;
       }
     }
     if (e_hi > e_lo) my_take[cw] = cur;
   }
   xsum[tid] = sum_h;
-  named_barrier(bar_id, kEpiThreads);
+  xcnt[tid] = n_thr;
+  named_barrier(bar_id, NT);
 
-  int bi[KS];
+  float sum = 1.f;
+  bool fast = false;
+  if (valid) {
+    sum = 0.f;
+    int thr_experts = 0;
 #pragma unroll
-  for (int j = 0; j < KS; ++j) bi[j] = -1;
+    for (int hh = 0; hh < Q; ++hh) {
+      sum += xsum[hh * kRouteBlock + r];
+      thr_experts += xcnt[hh * kRouteBlock + r];
+    }
+    bool distinct = true;
+#pragma unroll
+    for (int j = 0; j + 1 < KS; ++j)
+      if (j + 1 < k) distinct = distinct && bv[j] > bv[j + 1];
+    fast = distinct && thr_experts == 1;
+  }
+  if (fast) {
+    // slot j holds value bv[j]; the renormalised variant divides by the chosen gates' sum in
+    // slot order
+    float chosen = 0.f;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) chosen += j < k ? expf(bv[j] - m) / sum : 0.f;
+    for (int w = e_lo >> 5; w <= (e_hi - 1) >> 5 && e_hi > e_lo; ++w) {
+      uint32_t take = my_take[w];
+      while (take) {
+        const int e = w * 32 + __ffs(take) - 1;
+        take &= take - 1u;
+        const float v = fmaxf(ld_shared_f32(zr + 4u * (uint32_t)e), -INFINITY);
+        int pos = 0;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) pos += (j < k && bv[j] > v) ? 1 : 0;
+        const float gate = expf(v - m) / sum;
+        slotv[r * kMaxTopK + pos] = e;
+        ws.topk_idx[t * k + pos] = e;
+        ws.topk_gate[t * k + pos] = s.renorm ? gate / chosen : gate;
+        atomicOr(&mask_s[e * 4 + (r >> 5)], 1u << (r & 31));
+      }
+    }
+  }
   if (h == 0) {
-    float sum = 1.f;
-    if (valid) {
-      sum = xsum[r] + xsum[kRouteBlock + r];
+    if (valid && !fast) {
+      int bi[KS];
+#pragma unroll
+      for (int j = 0; j < KS; ++j) bi[j] = -1;
       uint32_t filled = 0u;
-      const uint32_t* t0w = xtake + r * 8;
-      const uint32_t* t1w = xtake + (kRouteBlock + r) * 8;
       for (int w = 0; w < (E + 31) / 32; ++w) {
-        uint32_t take = t0w[w] | t1w[w];
+        uint32_t take = 0u;
+#pragma unroll
+        for (int hh = 0; hh < Q; ++hh) take |= xtake[(hh * kRouteBlock + r) * 8 + w];
         while (take) {
           const int e = w * 32 + __ffs(take) - 1;
           take &= take - 1u;
@@ -283,6 +354,7 @@ __device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, in
       for (int j = 0; j < KS; ++j) {
         if (j < k) {
           const int e = bi[j];
+          slotv[r * kMaxTopK + j] = e;
           ws.topk_idx[t * k + j] = e;
           ws.topk_gate[t * k + j] = s.renorm ? gate[j] / chosen : gate[j];
           atomicOr(&mask_s[e * 4 + (r >> 5)], 1u << (r & 31));
@@ -292,50 +364,47 @@ __device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, in
     m_s[r] = valid ? m : 0.f;
     inv_s[r] = 1.f / sum;
   }
-  named_barrier(bar_id, kEpiThreads);
+  named_barrier(bar_id, NT);
 
-  if (h == 0 && valid) {
+  // ranks of the token's slots, split over its Q threads
+  if (valid) {
     const uint32_t below = (1u << (r & 31)) - 1u;
-#pragma unroll
-    for (int j = 0; j < KS; ++j) {
-      if (j < k) {
-        const uint32_t* mk = mask_s + bi[j] * 4;
-        int rank = __popc(mk[r >> 5] & below);
-        for (int wd = 0; wd < (r >> 5); ++wd) rank += __popc(mk[wd]);
-        ws.local_rank[t * k + j] = rank;
-      }
+    for (int j = h; j < k; j += Q) {
+      const uint32_t* mk = mask_s + slotv[r * kMaxTopK + j] * 4;
+      int rank = __popc(mk[r >> 5] & below);
+      for (int wd = 0; wd < (r >> 5); ++wd) rank += __popc(mk[wd]);
+      ws.local_rank[t * k + j] = rank;
     }
   }
-  for (int e = tid; e < E; e += kEpiThreads) {
+  for (int e = tid; e < E; e += NT) {
     const uint32_t* mk = mask_s + e * 4;
     ws.blk_cnt[(int64_t)blk * E + e] = __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
   }
-  // per-expert sums of p = exp(z - max) / sum over the block's rows (rows past T add 0)
+  // per-expert sums of p = q / sum over the block's rows (rows past T add 0)
   const int w8 = tid >> 5, lane = tid & 31;
   const int64_t t_base = (int64_t)blk * kRouteBlock;
-  float mrow[4], inv[4];
+  float inv[4];
   bool vrow[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    mrow[j] = m_s[lane + 32 * j];
     inv[j] = inv_s[lane + 32 * j];
     vrow[j] = t_base + lane + 32 * j < s.T;
   }
-  const uint32_t zc = static_cast<uint32_t>(__cvta_generic_to_shared(z_s + lane * ldz));
-  for (int e0 = 4 * w8; e0 < E; e0 += 32) {
-    float zz[4][4];
+  const uint32_t qc = static_cast<uint32_t>(__cvta_generic_to_shared(qs + lane * ldz));
+  for (int e0 = 4 * w8; e0 < E; e0 += 4 * (NT / 32)) {
+    float qq[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        zz[j][u] = e0 + u < E ? ld_shared_f32(zc + 4u * (uint32_t)(32 * j * ldz + e0 + u)) : 0.f;
+        qq[j][u] = (vrow[j] && e0 + u < E) ? ld_shared_f32(qc + 4u * (uint32_t)(32 * j * ldz + e0 + u)) : 0.f;
     float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int row = lane + 32 * j;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float p = vrow[j] ? expf(fmaxf(zz[j][u], -INFINITY) - mrow[j]) * inv[j] : 0.f;
+        const float p = vrow[j] ? qq[j][u] * inv[j] : 0.f;
         if (s.training && vrow[j] && e0 + u < E) ws.probs[(t_base + row) * E + e0 + u] = p;
         ps[u] += p;
       }
@@ -351,17 +420,20 @@ __device__ __forceinline__ void route_finish2_k(const Shape& s, const Ws& ws, in
   }
 }
 
-__device__ __forceinline__ void route_finish2(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo, int e_hi,
+template <int Q>
+__device__ __forceinline__ void route_finishq(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo, int e_hi,
                                               float* z_s, int ldz, uint32_t* mask_s, int bar_id) {
-  if (s.k <= 2) route_finish2_k<2>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
-  else if (s.k <= 4) route_finish2_k<4>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
-  else if (s.k <= 8) route_finish2_k<8>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
-  else route_finish2_k<kMaxTopK>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  if (s.k <= 2) route_finishq_k<2, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  else if (s.k <= 4) route_finishq_k<4, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  else if (s.k <= 8) route_finishq_k<8, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+  else route_finishq_k<kMaxTopK, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                             const __grid_constant__ CUtensorMap tmW, Shape s, Ws ws,
-                                                             Weights w, RouteGeom g, int64_t timeout_ns) {
+template <int Q>
+__global__ void __launch_bounds__(route_threads(Q), Q == 2 ? 2 : 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, Shape s, Ws ws,
+                    Weights w, RouteGeom g, int64_t timeout_ns) {
+  constexpr int NE = Q * kRouteBlock;  // epilogue threads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* body = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   RouteCtl* ctl = reinterpret_cast<RouteCtl*>(body + g.body_bytes);
@@ -464,18 +536,17 @@ __global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(const __grid_cons
     // two warps of a lane quarter take the two halves of the expert columns
     const int ew = warp - 2;
     const int q = warp & 3;
-    const int h = ew >> 2;
+    const int h = ew >> 2;        // expert range of this warp, 0..Q-1
     const int r = q * 32 + lane;  // token row of this block
-    const int eh = expert_half_split(g.e_pad);
-    const int c_lo = h == 0 ? 0 : eh, c_hi = h == 0 ? eh : g.e_pad;  // this warp's 16-column chunks
-    for (int e = ew * 32 + lane; e < g.e_pad; e += kEpiThreads) bias_s[e] = (s.has_bias && e < s.E) ? w.bias[e] : 0.f;
+    const int c_lo = range_col(g.e_pad, h, Q), c_hi = range_col(g.e_pad, h + 1, Q);  // its 16-column chunks
+    for (int e = ew * 32 + lane; e < g.e_pad; e += NE) bias_s[e] = (s.has_bias && e < s.E) ? w.bias[e] : 0.f;
     bool ok = ptx::mbar_wait(ptx::smem_u32(&ctl->tfull), 0u, timeout_ns, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (lane == 0) ctl->vote[ew] = ok ? 1 : 0;
-    named_barrier(2, kEpiThreads);
+    named_barrier(2, NE);
     bool all_ok = true;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) all_ok = all_ok && ctl->vote[i];
+    for (int i = 0; i < 4 * Q; ++i) all_ok = all_ok && ctl->vote[i];
     float* z_s = reinterpret_cast<float*>(body);
     const int ldz = s.E + 1;
     const bool finish_here = g.split == 1;
@@ -536,9 +607,8 @@ __global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(const __grid_cons
     const int q = warp & 3;
     const int h = ew >> 2;
     const int r = q * 32 + lane;
-    const int eh = expert_half_split(g.e_pad);
-    const int e_lo = h == 0 ? 0 : eh;
-    const int e_hi = h == 0 ? (eh < s.E ? eh : s.E) : s.E;
+    const int e_lo = min(range_col(g.e_pad, h, Q), s.E);
+    const int e_hi = min(range_col(g.e_pad, h + 1, Q), s.E);
     float* z_s = reinterpret_cast<float*>(body);
     uint32_t* mask_s = reinterpret_cast<uint32_t*>(z_s + kRouteBlock * (s.E + 1));
     const int ldz = s.E + 1;
@@ -563,9 +633,9 @@ __global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(const __grid_cons
         for (int i = 0; i < 16; ++i)
           if (i < n) st_shared_f32(z_row + 4u * (uint32_t)(c + i), finish_logit(z[i], b[i], s.tau));
       }
-      named_barrier(1, kEpiThreads);  // the other half's finished logits are in z_s too
+      named_barrier(1, NE);  // the other ranges' finished logits are in z_s too
     }
-    route_finish2(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, /*bar_id=*/1);
+    route_finishq<Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, /*bar_id=*/1);
   }
 
   __syncthreads();
@@ -585,6 +655,8 @@ __global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(const __grid_cons
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, g.tmem_cols);
   }
+  // the token blocks' leaders count themselves in; the last one runs the scan in its body
+  if (rank == 0) route_scan_if_last(s, ws, route_threads(Q), s.nblk, body);
 }
 
 }  // namespace
@@ -596,11 +668,11 @@ cudaError_t launch_route_tc(const Shape& s, const Ws& ws, const Weights& w, int 
   cudaError_t e;
   if ((e = make_tmap_bf16(&mx, w.x, (uint64_t)s.T, (uint64_t)s.d, kRouteBlock)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16(&mw, w.wr, (uint64_t)s.E, (uint64_t)s.d, (uint32_t)g.e_pad)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem)) !=
-      cudaSuccess)
+  auto kernel = g.q == 4 ? route_tc_kernel<4> : route_tc_kernel<2>;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem)) != cudaSuccess)
     return e;
-  return launch_kernel(route_tc_kernel, dim3((unsigned)(s.nblk * g.split)), dim3(kThreads), g.smem, st, false, g.split,
-                       mx, mw, s, ws, w, g, timeout_ns);
+  return launch_kernel(kernel, dim3((unsigned)(s.nblk * g.split)), dim3((unsigned)route_threads(g.q)), g.smem, st, false,
+                       g.split, mx, mw, s, ws, w, g, timeout_ns);
 }
 
 }  // namespace moe

@@ -32,10 +32,16 @@ class MoeConfig(ctypes.Structure):
                 ("wait_timeout_ns", ctypes.c_int64)]
 
 
+class MoeExpertConfig(ctypes.Structure):
+    _fields_ = [("max_rows", ctypes.c_int64), ("d_model", ctypes.c_int32), ("n_local_experts", ctypes.c_int32),
+                ("n_sources", ctypes.c_int32), ("d_expert", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
+                ("path", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_int64)]
+
+
 class MoeViews(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "status", "aux", "topk_idx", "topk_gate", "expert_counts", "expert_offsets", "perm_src",
-        "perm_slot", "gate_perm", "slot_pos", "logits", "xp", "h", "yp")]
+        "perm_slot", "gate_perm", "slot_pos", "logits", "xp", "h", "yp", "expert_psum")]
 
 
 _P = ctypes.c_void_p
@@ -71,6 +77,12 @@ _lib.moe_backward_stage_name.argtypes = [_P, ctypes.c_int32]
 _lib.moe_backward_stage_name.restype = ctypes.c_char_p
 _lib.moe_route_noalloc.argtypes = [_P] * 9 + [_P]
 _lib.moe_route_noalloc.restype = ctypes.c_int
+_lib.moe_expert_plan.argtypes = [ctypes.POINTER(MoeExpertConfig), ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]
+_lib.moe_expert_plan.restype = ctypes.c_int
+_lib.moe_expert_forward.argtypes = [_P] * 9 + [ctypes.c_size_t, _P]
+_lib.moe_expert_forward.restype = ctypes.c_int
+_lib.moe_aux_from_totals.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]
+_lib.moe_aux_from_totals.restype = ctypes.c_int
 _lib.moe_last_error.argtypes = []
 _lib.moe_last_error.restype = ctypes.c_char_p
 
@@ -227,4 +239,55 @@ class MoEPlan:
             perm_src=view(v.perm_src, i32, (N,)), perm_slot=view(v.perm_slot, i32, (N,)),
             gate_perm=view(v.gate_perm, f32, (N,)), slot_pos=view(v.slot_pos, i32, (N,)),
             logits=view(v.logits, f32, (self.T, self.E)), xp=view(v.xp, act, (N, self.d)),
-            h=view(v.h, act, (N, self.F)), yp=view(v.yp, act, (N, self.d)))
+            h=view(v.h, act, (N, self.F)), yp=view(v.yp, act, (N, self.d)),
+            expert_psum=view(v.expert_psum, f32, (self.E,)))
+
+
+class ExpertPlan:
+    """The expert stage of expert parallelism (moe_expert_plan / moe_expert_forward): the
+    local experts (E_l of them) on rows received from W sources, W * E_l segments in
+    source-major order, at most max_rows rows."""
+
+    def __init__(self, max_rows, d, E_local, n_sources, F, dtype="bf16", path="auto", wait_timeout_ns=0):
+        act = MOE_BF16 if dtype == "bf16" else MOE_F32
+        self.cfg = MoeExpertConfig(int(max_rows), int(d), int(E_local), int(n_sources), int(F), act, _PATHS[path],
+                                   int(wait_timeout_ns))
+        self.max_rows, self.d, self.E_local, self.n_sources, self.F = int(max_rows), int(d), int(E_local), \
+            int(n_sources), int(F)
+        self.act_dtype = _TORCH[act]
+        self._h = ctypes.c_void_p()
+        wsb = ctypes.c_size_t(0)
+        _check(_lib.moe_expert_plan(ctypes.byref(self.cfg), ctypes.byref(self._h), ctypes.byref(wsb)),
+               "moe_expert_plan")
+        self.workspace_bytes = wsb.value
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value:
+            _lib.moe_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    @property
+    def handle(self):
+        return self._h
+
+    def new_workspace(self, device="cuda"):
+        return torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device)
+
+    def forward(self, seg_counts, x_rows, gates, w1, w3, w2, y_rows, workspace, stream=None):
+        _check(_lib.moe_expert_forward(self._h, _ptr(seg_counts), _ptr(x_rows), _ptr(gates), _ptr(w1), _ptr(w3),
+                                       _ptr(w2), _ptr(y_rows), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "moe_expert_forward")
+
+    def device_status(self, workspace, stream=None):
+        """Synchronises the stream; returns the status code (MOE_OK == 0)."""
+        return _lib.moe_get_device_status(self._h, _ptr(workspace), _stream(stream))
+
+
+def aux_from_totals(E, k, T, counts, psum, out=None, stream=None):
+    """The balancing scalar from per-expert totals (moe_aux_from_totals): counts [E] int32 and
+    psum [E] fp32 on the device; returns a device fp32 scalar."""
+    if out is None:
+        out = torch.empty((), dtype=torch.float32, device=counts.device)
+    _check(_lib.moe_aux_from_totals(int(E), int(k), int(T), _ptr(counts), _ptr(psum), _ptr(out), _stream(stream)),
+           "moe_aux_from_totals")
+    return out

@@ -5,9 +5,8 @@ an MoE layer per operator -- dense and grouped GEMMs, data movement, dispatch la
 and reports how well that predicts measured utilisation.  This module does the same for the
 kernels of this library, from quantities the layer shape and the routing fix:
 
-  mover kernels (router, permute, combine):  t = L + bytes / B
-  scan:                                      t = L_scan + c_scan * ceil(T/128) * E
-  grouped GEMMs:                             t = L + FLOP_padded / (R * wave_efficiency)
+  mover kernels (router with its scan, permute, combine):  t = L + bytes / B
+  grouped GEMMs:                                           t = L + FLOP_padded / (R * wave_efficiency)
 
 FLOP_padded counts the rows the tensor cores actually process (256-row CTA-pair tiles of
 each expert, so padding and odd m-tiles count), and wave_efficiency = tiles / (slots *
@@ -19,7 +18,7 @@ import math
 
 import numpy as np
 
-STAGES = ("route", "scan", "permute", "gemm1_swiglu", "gemm2_gate", "combine")
+STAGES = ("route", "permute", "gemm1_swiglu", "gemm2_gate", "combine")
 PAIR_ROWS = 256      # rows of one CTA-pair tile
 GROUP_MTILES = 8     # 128-row m-tiles per scheduling group
 GEMM1_TILE_N = 128   # output columns of a SwiGLU tile (W1 and W3 halves)
@@ -48,7 +47,6 @@ def features(shape, counts, slots=76):
     wave = lambda n: n / (slots * math.ceil(n / slots)) if n else 1.0
     return {
         "route": T * d * 2 + N * 8,
-        "scan": math.ceil(T / 128) * E,
         "permute": T * d * 2 + N * d * 2 + 28 * N,
         "gemm1_swiglu": 4.0 * rows * d * F / wave(t1),
         "gemm2_gate": 2.0 * rows * d * F / wave(t2),

@@ -92,10 +92,11 @@ def test_backward_matches_oracle(dims, alpha, renorm, bias, path):
 def test_backward_full_size_coarse_e8():
     """The coarse-expert workload at full size (T=4096, d=2048, E=8, k=2, F=8192, its own
     seed-0 inputs, as the training-step benchmark runs it) with the balancing-loss term on.
-    About 1024 routed rows per expert: every expert spans a whole group of eight 128-row
-    m-tiles (the pair kernels' scheduling unit), the weight-gradient GEMMs run K over the
-    expert's rows with a partial last block, dH / dX run K = d and F at full size, and the
-    persistent grids take several waves.  Every element of every gradient is compared."""
+    About 1024 routed rows per expert: every expert spans eight or nine 128-row m-tiles (four
+    or five CTA-pair tiles, the last one half empty for odd counts), the weight-gradient GEMMs
+    run K over the expert's rows with a partial last block, dH / dX run K = d and F at full
+    size, and the persistent grids take several waves.  Every element of every gradient is
+    compared."""
     import time
     from top_routing_grouped_gb300 import moe
     from top_routing_grouped_gb300.workloads import SHAPES
@@ -119,7 +120,7 @@ def test_backward_full_size_coarse_e8():
     nerrs = {n: norm_err(got[n], ref[n]) for n in names}
     print(f"\n[backward coarse_e8 full size, rows/expert {counts.min()}..{counts.max()}, oracle {secs:.0f} s on "
           f"{oracle.num_threads()} threads] " + " ".join(f"{n}={errs[n]:.2e}/{nerrs[n]:.2e}" for n in names))
-    assert counts.min() >= 8 * 128 - 128, "every expert should span about a whole group of eight m-tiles"
+    assert counts.min() >= 7 * 128, "every expert should span seven or more m-tiles"
     for n in names:
         assert errs[n] <= TOL, f"{n}: {errs[n]}"
         assert nerrs[n] <= NORM_TOL, f"{n}: norm-wise {nerrs[n]}"

@@ -51,9 +51,10 @@ def test_fit_never_returns_a_negative_latency():
 
 @pytest.mark.parametrize("counts, pairs", [
     ([0], 0), ([1], 1), ([128], 1), ([129], 1), ([256], 1), ([257], 2),
-    ([1024], 4),               # 8 m-tiles: one whole group of 4 pairs
-    ([1025], 5),               # 9 m-tiles: a whole group, then a group of one m-tile (one pair)
-    ([8 * 128 * 3 + 3 * 128], 14),   # 27 m-tiles: 3 groups of 4 pairs + a group of 3 (2 pairs)
+    ([1024], 4),               # 8 m-tiles: 4 pairs
+    ([1025], 5),               # 9 m-tiles: 4 whole pairs and a half-empty one
+    ([16 * 128 + 128], 9),     # 17 m-tiles: a whole group of 16 (8 pairs), then a group of one m-tile
+    ([16 * 128 * 3 + 3 * 128], 26),  # 51 m-tiles: 3 groups of 8 pairs + a group of 3 (2 pairs)
     ([0, 1, 0, 300, 2048], 1 + 2 + 8),
 ])
 def test_pair_tiles_closed_forms(counts, pairs):
@@ -69,6 +70,9 @@ def test_features_charge_padding_and_the_last_wave():
     eff = t1 / (76 * math.ceil(t1 / 76))
     assert f["gemm1_swiglu"] == pytest.approx(4.0 * pairs * 256 * s.d * s.F / eff)
     assert f["gemm1_swiglu"] >= 4.0 * s.N * s.d * s.F
+    # one row more in the first expert: a ninth m-tile, i.e. a fifth, half-empty pair
+    f2 = pm.features(s, [counts[0] + 1] + counts[1:-1] + [counts[-1] - 1])
+    assert f2["gemm1_swiglu"] > f["gemm1_swiglu"]
     assert f["route"] == s.T * s.d * 2 + s.N * 8
 
 
@@ -93,5 +97,7 @@ def test_pair_tiles_match_the_scan_kernel(shape):
     hdr = v["status"].cpu().numpy()
     assert counts.sum() == shape.N
     assert pm.pair_tiles(counts) == int(hdr[4]), (pm.pair_tiles(counts), int(hdr[4]))
+    mt = (counts.astype(np.int64) + 127) // 128
+    assert int(hdr[3]) == mt.sum()
     del ws
     torch.cuda.empty_cache()

@@ -12,80 +12,33 @@
 // rows of one expert that came from different sources never share a tile, and nothing is
 // copied into expert order first.
 #include "device_common.cuh"
+#include "tile_tables.cuh"
 
 namespace moe {
 
 constexpr int kSegThreads = kMaxExperts;  // one thread per segment (W * E_l <= 256)
 
-// One CTA: segment counts (device input) -> counts, offsets, tile descriptors, header totals.
-// A negative count or a total beyond the plan's row capacity is reported (MOE_ERR_INTERNAL,
-// site 0x700) and leaves an empty tile table, so that no GEMM reads outside the buffers.
+// One CTA: segment counts (device input) -> counts, offsets, tile tables, header totals.  A
+// negative count or a total beyond the plan's row capacity is reported (MOE_ERR_INTERNAL, site
+// 0x740) and leaves empty tile tables, so that no GEMM reads outside the buffers.
 __global__ void __launch_bounds__(kSegThreads) seg_scan_kernel(Shape s, Ws ws, const int32_t* seg_counts, int n_seg,
                                                                int n_local) {
-  __shared__ int wtot[4][kSegThreads / 32];  // warp totals of count, m-tiles, groups, pairs
-  const int i = threadIdx.x, lane = i & 31, w = i >> 5;
+  __shared__ int cnt_s[kMaxExperts], offs_s[kMaxExperts];
+  __shared__ int scratch[kTileScratchInts];
+  const int i = threadIdx.x;
   int cnt = i < n_seg ? seg_counts[i] : 0;
   const bool neg = cnt < 0;
-  if (neg) cnt = 0;
-  const int mt = (cnt + kTileM - 1) / kTileM;
-  const int ng = (mt + kGroupM - 1) / kGroupM;
-  const int last_gm = mt - (ng - 1) * kGroupM;
-  const int np = ng > 0 ? (ng - 1) * (kGroupM / 2) + (last_gm + 1) / 2 : 0;
-  const int own[4] = {cnt, mt, ng, np};
-  int incl[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    int v = own[q];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
-    }
-    incl[q] = v;
-    if (lane == 31) wtot[q][w] = v;
-  }
-  const bool any_neg = __syncthreads_or(neg);
-  int base[4], total[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    base[q] = 0;
-    total[q] = 0;
-    for (int ww = 0; ww < kSegThreads / 32; ++ww) {
-      if (ww < w) base[q] += wtot[q][ww];
-      total[q] += wtot[q][ww];
-    }
-  }
-  const int n_rows = total[0], n_mtiles = total[1], n_groups = total[2], n_pairs = total[3];
-  if (any_neg || n_rows > s.N || n_groups > s.max_groups) {
+  cnt_s[i] = neg ? 0 : cnt;
+  if (__syncthreads_or(neg)) {
     if (i == 0) {
-      record_error(ws, MOE_ERR_INTERNAL, 0x700u);
+      record_error(ws, MOE_ERR_INTERNAL, 0x740u);
       ws.hdr[kHdrNumGroups] = 0;
       ws.hdr[kHdrNumMTiles] = 0;
       ws.hdr[kHdrNumPairs] = 0;
     }
     return;
   }
-  if (i < n_seg) {
-    const int off = base[0] + incl[0] - cnt;
-    const int mstart = base[1] + incl[1] - mt, pstart = base[3] + incl[3] - np;
-    const int we = i % n_local;  // the segment's local expert: the weight index of its tiles
-    ws.counts[i] = cnt;
-    ws.offsets[i] = off;
-    for (int g = 0; g < ng; ++g) {
-      const int gm = g + 1 < ng ? kGroupM : last_gm;
-      const int gp = (gm + 1) / 2;
-      const int m0 = mstart + g * kGroupM, p0 = pstart + g * (kGroupM / 2);
-      const int row0 = off + g * kGroupM * kTileM;
-      for (int j = 0; j < gm; ++j) ws.mt_desc[m0 + j] = make_int4(we | (gm << 20), m0, row0, off + cnt);
-      for (int j = 0; j < gp; ++j) ws.pr_desc[p0 + j] = make_int4(we | (gp << 20), p0, row0, off + cnt);
-    }
-  }
-  if (i == 0) {
-    ws.offsets[n_seg] = n_rows;
-    ws.hdr[kHdrNumGroups] = (uint32_t)n_groups;
-    ws.hdr[kHdrNumMTiles] = (uint32_t)n_mtiles;
-    ws.hdr[kHdrNumPairs] = (uint32_t)n_pairs;
-  }
+  build_tile_tables(s, ws, n_seg, n_local, cnt_s, offs_s, scratch, kSegThreads, /*exact=*/false, 0x740u);
 }
 
 cudaError_t launch_seg_scan(const Shape& s, const Ws& ws, const int32_t* seg_counts, int n_seg, int n_local,

@@ -9,7 +9,7 @@ namespace moe {
 
 constexpr int kRouteBlock = 128;   // tokens per router CTA (= rows of one router MMA tile)
 constexpr int kTileM = 128;        // rows per expert-GEMM m-tile
-constexpr int kGroupM = 8;         // m-tiles per scheduling group (weight-tile reuse in L2)
+constexpr int kGroupM = 16;        // m-tiles per scheduling group (weight-tile reuse in L2)
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 256;
 

@@ -19,6 +19,7 @@
 // result is the same on every run.
 #pragma once
 #include "device_common.cuh"
+#include "tile_tables.cuh"
 
 namespace moe {
 
@@ -41,10 +42,10 @@ __host__ __device__ inline ScanSplit scan_split(const Shape& s, int nt) {
 }
 
 // Shared-memory bytes the scan needs when run by nt threads: per-(chunk, expert) counts and
-// sums of p, the four per-expert scan columns, warp totals, the aux tree and the totals.
+// sums of p, per-expert counts, offsets, sums of p and aux terms, and the tile tables' scratch.
 __host__ __device__ inline size_t route_scan_smem(const Shape& s, int nt) {
   const ScanSplit p = scan_split(s, nt);
-  return (size_t)p.chunks * s.E * 8 + 4 * kMaxExperts * 4 + 4 * 8 * 4 + 4 * kMaxExperts * 4 + 16;
+  return (size_t)p.chunks * s.E * 8 + 4 * kMaxExperts * 4 + (size_t)kTileScratchInts * 4 + 16;
 }
 
 // Called by every thread (nt of them) of every router CTA that wrote a token block's outputs,
@@ -65,13 +66,11 @@ static __device__ __noinline__ bool route_scan_if_last(const Shape& s, const Ws&
   const ScanSplit sp = scan_split(s, nt);
   int* ccnt = static_cast<int*>(scratch);                             // [chunks][E]
   float* cps = reinterpret_cast<float*>(ccnt + sp.chunks * E);       // [chunks][E]
-  int* col = reinterpret_cast<int*>(cps + sp.chunks * E);            // [4][256]: cnt, m-tiles, groups, pairs
-  int* wtot = col + 4 * kMaxExperts;                                 // [4][8] warp totals
-  float* red = reinterpret_cast<float*>(wtot + 32);                  // [256] aux terms
-  float* tps = red + kMaxExperts;                                    // [256] sums of p per expert
-  int* rawc = reinterpret_cast<int*>(tps + kMaxExperts);             // [256] counts per expert
+  int* rawc = reinterpret_cast<int*>(cps + sp.chunks * E);           // [256] counts per expert
   int* offs = rawc + kMaxExperts;                                    // [256] offsets per expert
-  int* tot = offs + kMaxExperts;                                     // [4] totals of the four columns
+  float* tps = reinterpret_cast<float*>(offs + kMaxExperts);         // [256] sums of p per expert
+  float* red = tps + kMaxExperts;                                    // [256] aux terms
+  int* tile_scratch = reinterpret_cast<int*>(red + kMaxExperts);     // kTileScratchInts
 
   // pass A: per-(chunk, expert) sums of the counts and of p, blocks in order (eight blocks'
   // loads in flight at a time)
@@ -126,7 +125,7 @@ static __device__ __noinline__ bool route_scan_if_last(const Shape& s, const Ws&
     }
   }
   __syncthreads();
-  // per expert: totals, and chunk prefixes in chunk order; the four scan columns
+  // per expert: totals, and chunk prefixes in chunk order
   for (int e = tid; e < kMaxExperts; e += nt) {
     int cnt = 0;
     float ps = 0.f;
@@ -137,122 +136,20 @@ static __device__ __noinline__ bool route_scan_if_last(const Shape& s, const Ws&
         cnt += v;
         ps += cps[c * E + e];
       }
-    const int mt = (cnt + kTileM - 1) / kTileM;  // m-tiles
-    const int ng = (mt + kGroupM - 1) / kGroupM;  // scheduling groups
-    // m-tile pairs: ceil(gm / 2) per group; every group but an expert's last holds kGroupM
-    const int last_gm = mt - (ng - 1) * kGroupM;
-    const int np = ng > 0 ? (ng - 1) * (kGroupM / 2) + (last_gm + 1) / 2 : 0;
     rawc[e] = cnt;
-    col[e] = cnt;
-    col[kMaxExperts + e] = mt;
-    col[2 * kMaxExperts + e] = ng;
-    col[3 * kMaxExperts + e] = np;
     tps[e] = ps;
   }
   __syncthreads();
-  // exclusive scans of the four columns over the 256 expert slots: a warp scan per 32 slots,
-  // then the warp totals in order
-  const int lane = tid & 31, nw = nt >> 5;
-  for (int w = tid >> 5; w < kMaxExperts / 32; w += nw) {
-    const int e = w * 32 + lane;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      int v = col[q * kMaxExperts + e];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-      }
-      col[q * kMaxExperts + e] = v;  // inclusive within the warp
-      if (lane == 31) wtot[q * 8 + w] = v;
-    }
-  }
-  __syncthreads();
-  if (tid < 4) {
-    int run = 0;
-    for (int w = 0; w < 8; ++w) {
-      const int v = wtot[tid * 8 + w];
-      wtot[tid * 8 + w] = run;
-      run += v;
-    }
-    tot[tid] = run;
-  }
-  __syncthreads();
-  const int n_routed = tot[0], n_mtiles = tot[1], n_groups = tot[2], n_pairs = tot[3];
-  if (n_routed != s.N || n_groups > s.max_groups) {
-    if (tid == 0) {
-      record_error(ws, MOE_ERR_INTERNAL, 0x200u);
-      ws.hdr[kHdrNumGroups] = 0;
-      ws.hdr[kHdrNumMTiles] = 0;
-      ws.hdr[kHdrNumPairs] = 0;
-    }
-    return true;
-  }
-  // per expert: counts, offsets, first m-tile and pair, aux terms (exclusive = inclusive - own)
-  int* mst = col;                    // the m-tile columns are no longer needed: first m-tile of each expert,
-  int* pst = col + kMaxExperts;      // first pair of each expert (over the count column's slots)
-  __syncthreads();
+  // counts, offsets, tile tables, header totals; every routed row must be counted once
+  if (build_tile_tables(s, ws, E, E, rawc, offs, tile_scratch, nt, /*exact=*/true, 0x200u) < 0) return true;
   for (int e = tid; e < kMaxExperts; e += nt) {
     float term = 0.f;
-    int mstart = 1 << 30, pstart = 1 << 30;
     if (e < E) {
-      const int w = e >> 5;
-      const int cnt = rawc[e];
-      const int mt = (cnt + kTileM - 1) / kTileM;
-      const int ng = (mt + kGroupM - 1) / kGroupM;
-      const int last_gm = mt - (ng - 1) * kGroupM;
-      const int np = ng > 0 ? (ng - 1) * (kGroupM / 2) + (last_gm + 1) / 2 : 0;
-      const int off = col[e] + wtot[w] - cnt;
-      mstart = col[kMaxExperts + e] + wtot[8 + w] - mt;
-      pstart = col[3 * kMaxExperts + e] + wtot[24 + w] - np;
-      offs[e] = off;
-      ws.counts[e] = cnt;
-      ws.offsets[e] = off;
       if (ws.ptot) ws.ptot[e] = tps[e];
       // aux term f_e * P_e
-      term = ((float)cnt / ((float)s.T * (float)s.k)) * (tps[e] / (float)s.T);
+      term = ((float)rawc[e] / ((float)s.T * (float)s.k)) * (tps[e] / (float)s.T);
     }
     red[e] = term;
-    rawc[e] = mstart;  // reused below: first m-tile (the counts are in ws.counts and offs)
-    tps[e] = __int_as_float(pstart);
-  }
-  __syncthreads();
-  for (int e = tid; e < kMaxExperts; e += nt) {
-    mst[e] = rawc[e];
-    pst[e] = __float_as_int(tps[e]);
-  }
-  __syncthreads();
-  // tile descriptors, one thread per m-tile (then per pair): the owning expert is the last one
-  // whose first m-tile (pair) is at or below the index (binary search over the experts'
-  // non-decreasing starts; experts without tiles share their successor's start)
-  for (int q = tid; q < n_mtiles + n_pairs; q += nt) {
-    const bool pair = q >= n_mtiles;
-    const int idx = pair ? q - n_mtiles : q;
-    const int* st = pair ? pst : mst;
-    int lo = 0, hi = E - 1;  // largest e with st[e] <= idx
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (st[mid] <= idx) lo = mid;
-      else hi = mid - 1;
-    }
-    const int e = lo;
-    const int cnt = (e + 1 < E ? offs[e + 1] : n_routed) - offs[e];
-    const int mt = (cnt + kTileM - 1) / kTileM;
-    const int ng = (mt + kGroupM - 1) / kGroupM;
-    const int last_gm = mt - (ng - 1) * kGroupM;
-    const int local = idx - st[e];
-    const int g = pair ? local / (kGroupM / 2) : local / kGroupM;
-    const int gm = g + 1 < ng ? kGroupM : last_gm;
-    const int off = offs[e];
-    const int row0 = off + g * kGroupM * kTileM;
-    if (!pair) ws.mt_desc[idx] = make_int4(e | (gm << 20), mst[e] + g * kGroupM, row0, off + cnt);
-    else ws.pr_desc[idx] = make_int4(e | (((gm + 1) / 2) << 20), pst[e] + g * (kGroupM / 2), row0, off + cnt);
-  }
-  if (tid == 0) {
-    ws.offsets[E] = n_routed;
-    ws.hdr[kHdrNumGroups] = (uint32_t)n_groups;
-    ws.hdr[kHdrNumMTiles] = (uint32_t)n_mtiles;
-    ws.hdr[kHdrNumPairs] = (uint32_t)n_pairs;
   }
   __syncthreads();
   // aux = E * sum_e f_e P_e over a fixed tree

@@ -20,13 +20,14 @@ import numpy as np
 
 STAGES = ("route", "permute", "gemm1_swiglu", "gemm2_gate", "combine")
 PAIR_ROWS = 256      # rows of one CTA-pair tile
-GROUP_MTILES = 8     # 128-row m-tiles per scheduling group
+GROUP_MTILES = 16    # 128-row m-tiles per scheduling group
 GEMM1_TILE_N = 128   # output columns of a SwiGLU tile (W1 and W3 halves)
 GEMM2_TILE_N = 256
 
 
 def pair_tiles(counts):
-    """CTA-pair m-tiles per expert: groups of up to 8 m-tiles, ceil(m/2) pairs per group."""
+    """CTA-pair m-tiles per expert: groups of up to GROUP_MTILES m-tiles, ceil(m/2) pairs per
+    group (GROUP_MTILES is even, so this is ceil(m/2) per expert whatever the group size)."""
     pairs = 0
     for c in counts:
         mt = (int(c) + 127) // 128

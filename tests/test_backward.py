@@ -57,6 +57,8 @@ def run_backward(moe, s, inp, alpha, path="auto"):
     ((200, 192, 8, 3, 256), 0.25, True, True, "auto"),     # renormalised gates
     ((130, 128, 32, 2, 64), 0.0, False, False, "auto"),    # experts with 0..few rows (zero dW)
     ((1024, 1024, 8, 2, 1024), 0.1, False, True, "auto"),  # medium: many K blocks per expert, 4 H tiles
+    ((300, 128, 256, 16, 64), 0.1, False, False, "auto"),  # the most experts and the largest top-k
+    ((260, 128, 200, 8, 64), 0.0, True, True, "auto"),     # E above 128, not a multiple of 16
     # the one-CTA backward GEMMs (MOE_PATH_TC_1SM)
     ((300, 256, 8, 2, 192), 0.0, False, True, "tc1"),
     ((130, 128, 32, 2, 64), 0.0, False, False, "tc1"),

@@ -59,6 +59,21 @@ def test_small_bf16(moe, path, dims):
 
 
 @pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dims", [
+    (300, 256, 256, 16, 64),   # the most experts and the largest top-k the plan accepts
+    (200, 128, 200, 8, 64),    # E above 128 and not a multiple of 16 (four threads finish a token)
+    (100, 2048, 33, 3, 64),    # one token block, long d: d split over a cluster of four, deepest ring
+    (130, 4096, 160, 5, 64),   # many experts: the kept exp(z - max) no longer fits, the softmax sums recompute it
+], ids=lambda d: "x".join(map(str, d)))
+def test_maximum_sizes(moe, path, dims):
+    """The largest expert counts and top-k, and the router shapes whose shared memory is
+    tightest (split-d clusters with a receive buffer, many experts)."""
+    T, d, E, k, F = dims
+    s = small("maximum", T, d, E, k, F)
+    check(moe, s, make_inputs(s, seed=8), path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
 def test_temperature_and_bias(moe, path):
     s = small("tau_bias", 384, 256, 16, 4, 128, tau=0.5)
     inp = make_inputs(s, seed=2)

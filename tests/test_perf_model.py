@@ -43,10 +43,26 @@ def test_fit_recovers_known_latency_and_rate():
 
 def test_fit_never_returns_a_negative_latency():
     x = np.array([1.0, 2.0, 3.0, 4.0]) * 1e8
-    samples = [({st: v for st in pm.STAGES}, {st: 2e-9 * v - 0.05 for st in pm.STAGES}) for v in x]
+    y = 2e-9 * x - 0.05
+    samples = [({st: v for st in pm.STAGES}, {st: t for st in pm.STAGES}) for v, t in zip(x, y)]
+    # through the origin, relative errors: minimise sum((s x / y - 1)^2)
+    xw = x / y
     for L, slope in pm.fit(samples).values():
         assert L == 0.0
-        assert slope == pytest.approx(float((x @ (2e-9 * x - 0.05)) / (x @ x)), rel=1e-12)
+        assert slope == pytest.approx(float(xw.sum() / (xw @ xw)), rel=1e-12)
+
+
+def test_fit_weighs_layers_by_relative_error():
+    """Three layers a decade apart in size with +10 %, 0, -10 % deviations from one rate: the
+    fit keeps every layer's relative error under 5 %, where an unweighted least-squares fit
+    (dominated by the largest layer) misses the smallest by about 30 %."""
+    x = np.array([1e8, 1e9, 1e10])
+    y = np.array([1.1e-9 * 1e8, 1.0e-9 * 1e9, 0.9e-9 * 1e10]) + 0.02
+    samples = [({st: v for st in pm.STAGES}, {st: t for st in pm.STAGES}) for v, t in zip(x, y)]
+    L, slope = pm.fit(samples)["gemm1_swiglu"]
+    assert np.max(np.abs(L + slope * x - y) / y) < 0.05
+    (L0, s0), *_ = np.linalg.lstsq(np.stack([np.ones_like(x), x], axis=1), y, rcond=None)
+    assert np.max(np.abs(L0 + s0 * x - y) / y) > 0.25
 
 
 @pytest.mark.parametrize("counts, pairs", [

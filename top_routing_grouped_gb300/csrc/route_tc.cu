@@ -62,6 +62,8 @@ struct RouteGeom {
   int stages;
   int stage_bytes;  // x tile + W_r tile
   int body_bytes;   // max(stages * stage_bytes, logits + masks)
+  int keep_q;       // exp(z - max) of every logit kept in shared memory for the softmax sums
+                    // (when it fits; otherwise the sums recompute it)
   uint32_t tmem_cols;
   size_t smem;      // dynamic shared memory
 };
@@ -100,12 +102,19 @@ RouteGeom route_geom(const Shape& s, int num_sms) {
   g.stages = ((alone ? 192 : 96) * 1024) / g.stage_bytes;
   if (g.stages > kMaxStages) g.stages = kMaxStages;
   if (g.stages > g.kb_per) g.stages = g.kb_per;
+  // and no more than the shared memory left beside the control block, the cluster's receive
+  // buffer and the bias (227 KB per CTA)
+  const int fixed = 1024 + (int)sizeof(RouteCtl) + 16 + g.recv_bytes + g.e_pad * 4 + 1024;  // + static, slack
+  while (g.stages > 2 && g.stages * g.stage_bytes + fixed > 227 * 1024) --g.stages;
   if (g.stages < 2) g.stages = 2;
-  // logits, then the masks and per-row floats of the finish, then its pair exchange
-  // logits, masks and per-row floats, the exchange, then exp(z - max) per logit for the
-  // softmax sums
-  const int zs = 2 * kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4 + xchg_bytes(g.q);
-  g.body_bytes = g.stages * g.stage_bytes > zs ? g.stages * g.stage_bytes : zs;
+  // logits, masks and per-row floats, the exchange, then (if it fits) exp(z - max) per logit
+  // for the softmax sums
+  const int zs0 = kRouteBlock * (s.E + 1) * 4 + (4 * s.E + 2 * kRouteBlock) * 4 + xchg_bytes(g.q);
+  const int zs1 = zs0 + kRouteBlock * (s.E + 1) * 4;
+  const int ring = g.stages * g.stage_bytes;
+  g.keep_q = ((ring > zs1 ? ring : zs1) + 1023) / 1024 * 1024 + fixed <= 227 * 1024 ? 1 : 0;
+  const int zs = g.keep_q ? zs1 : zs0;
+  g.body_bytes = ring > zs ? ring : zs;
   // the scan of the last CTA reuses the body
   const int scan = (int)route_scan_smem(s, route_threads(g.q));
   if (g.body_bytes < scan) g.body_bytes = scan;
@@ -154,7 +163,8 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]
 //      lane, +32, +64, +96 in that order, then a fixed butterfly).
 template <int KS, int Q>
 __device__ __forceinline__ void route_finishq_k(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo,
-                                                int e_hi, float* z_s, int ldz, uint32_t* mask_s, int bar_id) {
+                                                int e_hi, float* z_s, int ldz, uint32_t* mask_s, int bar_id,
+                                                bool keep_q) {
   constexpr int NT = Q * kRouteBlock;
   const int E = s.E, k = s.k;
   const int tid = h * kRouteBlock + r;
@@ -243,7 +253,7 @@ __device__ __forceinline__ void route_finishq_k(const Shape& s, const Ws& ws, in
           cw = e >> 5;
         }
         const float q = expf(v4[u] - m);
-        st_shared_f32(qr + 4u * (uint32_t)e, q);
+        if (keep_q) st_shared_f32(qr + 4u * (uint32_t)e, q);
         sum_h += q;
         cur |= (v4[u] >= thr ? 1u : 0u) << (e & 31);
         n_thr += v4[u] == thr ? 1 : 0;
@@ -383,21 +393,25 @@ __device__ __forceinline__ void route_finishq_k(const Shape& s, const Ws& ws, in
   // per-expert sums of p = q / sum over the block's rows (rows past T add 0)
   const int w8 = tid >> 5, lane = tid & 31;
   const int64_t t_base = (int64_t)blk * kRouteBlock;
-  float inv[4];
+  float mrow[4], inv[4];
   bool vrow[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    mrow[j] = m_s[lane + 32 * j];
     inv[j] = inv_s[lane + 32 * j];
     vrow[j] = t_base + lane + 32 * j < s.T;
   }
-  const uint32_t qc = static_cast<uint32_t>(__cvta_generic_to_shared(qs + lane * ldz));
+  // q from pass 2, or recomputed from the logits when it was not kept (the same value)
+  const uint32_t qc = static_cast<uint32_t>(__cvta_generic_to_shared((keep_q ? qs : z_s) + lane * ldz));
   for (int e0 = 4 * w8; e0 < E; e0 += 4 * (NT / 32)) {
     float qq[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 4; ++u) {
         qq[j][u] = (vrow[j] && e0 + u < E) ? ld_shared_f32(qc + 4u * (uint32_t)(32 * j * ldz + e0 + u)) : 0.f;
+        if (!keep_q && vrow[j] && e0 + u < E) qq[j][u] = expf(fmaxf(qq[j][u], -INFINITY) - mrow[j]);
+      }
     float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -422,11 +436,11 @@ __device__ __forceinline__ void route_finishq_k(const Shape& s, const Ws& ws, in
 
 template <int Q>
 __device__ __forceinline__ void route_finishq(const Shape& s, const Ws& ws, int blk, int r, int h, int e_lo, int e_hi,
-                                              float* z_s, int ldz, uint32_t* mask_s, int bar_id) {
-  if (s.k <= 2) route_finishq_k<2, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
-  else if (s.k <= 4) route_finishq_k<4, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
-  else if (s.k <= 8) route_finishq_k<8, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
-  else route_finishq_k<kMaxTopK, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id);
+                                              float* z_s, int ldz, uint32_t* mask_s, int bar_id, bool keep_q) {
+  if (s.k <= 2) route_finishq_k<2, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id, keep_q);
+  else if (s.k <= 4) route_finishq_k<4, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id, keep_q);
+  else if (s.k <= 8) route_finishq_k<8, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id, keep_q);
+  else route_finishq_k<kMaxTopK, Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, bar_id, keep_q);
 }
 
 template <int Q>
@@ -635,7 +649,7 @@ __global__ void __launch_bounds__(route_threads(Q), Q == 2 ? 2 : 1)
       }
       named_barrier(1, NE);  // the other ranges' finished logits are in z_s too
     }
-    route_finishq<Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, /*bar_id=*/1);
+    route_finishq<Q>(s, ws, blk, r, h, e_lo, e_hi, z_s, ldz, mask_s, /*bar_id=*/1, g.keep_q != 0);
   }
 
   __syncthreads();

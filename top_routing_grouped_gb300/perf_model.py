@@ -57,15 +57,18 @@ def features(shape, counts, slots=76):
 
 def fit(samples):
     """samples: list of (features dict, measured stage_ms dict).  Returns, per stage, the
-    (L [ms], slope [ms per unit]) least-squares fit of t = L + slope * work (L >= 0)."""
+    (L [ms], slope [ms per unit]) fit of t = L + slope * work (L >= 0) that minimises the
+    squared RELATIVE errors, so that every layer weighs the same whatever its size."""
     params = {}
     for st in STAGES:
         x = np.array([f[st] for f, _ in samples], dtype=np.float64)
         y = np.array([m[st] for _, m in samples], dtype=np.float64)
-        A = np.stack([np.ones_like(x), x], axis=1)
-        (L, slope), *_ = np.linalg.lstsq(A, y, rcond=None)
+        w = 1.0 / y
+        A = np.stack([np.ones_like(x), x], axis=1) * w[:, None]
+        (L, slope), *_ = np.linalg.lstsq(A, y * w, rcond=None)
         if L < 0:  # a negative launch latency is not physical: refit through the origin
-            L, slope = 0.0, float((x @ y) / (x @ x))
+            xw, yw = x * w, y * w
+            L, slope = 0.0, float((xw @ yw) / (xw @ xw))
         params[st] = (float(L), float(slope))
     return params
 

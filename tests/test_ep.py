@@ -46,20 +46,15 @@ def emulate_all_to_all(outs, sends, splits):
         outs[j][:cat.shape[0]].copy_(cat)
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "T{}_d{}_E{}_k{}_F{}_W{}{}_{}".format(
-    *c[:6], "_zipf" if c[6] else "", c[8]))
-def test_expert_parallel_step_matches_the_oracle(case):
-    import oracle
+def run_ep(T, d, E, k, F, W, tau, path, inp):
+    """One expert-parallel step over W emulated ranks; returns (ranks, y [T,d] host fp64, aux, segs)."""
     import parity
     from top_routing_grouped_gb300 import moe
     from top_routing_grouped_gb300.ep import EPRank, rows_per_rank
-    T, d, E, k, F, W, zipf, tau, path = case
-    dtype = "bf16"
-    s = MoEShape("ep", T=T, d=d, E=E, k=k, F=F, dtype=dtype, tau=tau, zipf_bias=zipf)
-    inp = make_inputs(s, seed=5)
     dev = inp.to("cuda")
+    has_bias = inp.bias is not None
     Tl, El = T // W, E // W
-    ranks = [EPRank(Tl, d, E, k, F, W, r, dtype=dtype, tau=tau, has_bias=zipf, path=path) for r in range(W)]
+    ranks = [EPRank(Tl, d, E, k, F, W, r, dtype="bf16", tau=tau, has_bias=has_bias, path=path) for r in range(W)]
     xs = [dev.x[r * Tl:(r + 1) * Tl].contiguous() for r in range(W)]
     ys = [torch.empty(Tl, d, dtype=ranks[0].src.out_dtype, device="cuda") for _ in range(W)]
     w1 = [dev.w1[r * El:(r + 1) * El].contiguous() for r in range(W)]
@@ -88,10 +83,15 @@ def test_expert_parallel_step_matches_the_oracle(case):
         assert rk.src.device_status(rk.ws) == moe.MOE_OK
         assert rk.exp.device_status(rk.ws_exp) == moe.MOE_OK
     assert sum(sum(rc) for rc in recv) == T * k
+    y = np.concatenate([parity.to_np(yy) for yy in ys])
+    return ranks, y, aux, segs
 
-    # against the oracle of the whole layer
+
+def check_against_oracle(T, d, E, k, F, tau, inp, ranks, y, aux, full_tokens):
+    import oracle
+    import parity
     host = inp.numpy_for_oracle()
-    orc = oracle.Oracle(T, d, E, k, F, tau=tau, dtype=dtype)
+    orc = oracle.Oracle(T, d, E, k, F, tau=tau, dtype="bf16")
     z, p, oidx, _ = orc.router(host["x"], host["wr"], host["bias"])
     gidx = np.concatenate([rk.views["topk_idx"].cpu().numpy() for rk in ranks])
     ggate = np.concatenate([rk.views["topk_gate"].cpu().numpy() for rk in ranks]).astype(np.float64)
@@ -99,25 +99,50 @@ def test_expert_parallel_step_matches_the_oracle(case):
     np.testing.assert_array_equal(np.sort(gidx[clear], 1), np.sort(oidx[clear], 1))
     gref = np.take_along_axis(p, gidx, axis=1)
     assert np.max(np.abs(ggate - gref) / (gref + 1e-12)) <= parity.GATE_RTOL
-    y = np.concatenate([parity.to_np(yy) for yy in ys])
-    tokens = None if T * d * F <= (1 << 31) else np.unique(np.concatenate(
-        [np.arange(0, T, 17), np.arange(Tl - 40, Tl + 40)]))
+    Tl = T // len(ranks)
+    tokens = None if full_tokens else np.unique(np.concatenate([np.arange(0, T, 17), np.arange(Tl - 40, Tl + 40)]))
     yref = orc.combine(host["x"], host["w1"], host["w3"], host["w2"], gidx, gref, tokens)
     yg = y if tokens is None else y[tokens]
     err = np.abs(yg - yref) / (1 + np.abs(yref))
-    tol = parity.Y_TOL[dtype]
-    print(f"\n[ep {case}] y max err {err.max():.2e} on {yg.shape[0]} tokens; segments "
-          f"{[sg.cpu().tolist() for sg in segs]}")
-    assert err.max() <= tol
+    assert err.max() <= parity.Y_TOL["bf16"], err.max()
     counts_all, _, _, _ = orc.dispatch(gidx)
     aux_ref = orc.aux(p, counts_all)
     assert abs(aux - aux_ref) <= parity.AUX_RTOL * abs(aux_ref), (aux, aux_ref)
+    return float(err.max())
 
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "T{}_d{}_E{}_k{}_F{}_W{}{}_{}".format(
+    *c[:6], "_zipf" if c[6] else "", c[8]))
+def test_expert_parallel_step_matches_the_oracle(case):
+    import parity
+    from top_routing_grouped_gb300 import moe
+    T, d, E, k, F, W, zipf, tau, path = case
+    s = MoEShape("ep", T=T, d=d, E=E, k=k, F=F, dtype="bf16", tau=tau, zipf_bias=zipf)
+    inp = make_inputs(s, seed=5)
+    ranks, y, aux, segs = run_ep(T, d, E, k, F, W, tau, path, inp)
+    err = check_against_oracle(T, d, E, k, F, tau, inp, ranks, y, aux, full_tokens=T * d * F <= (1 << 31))
+    print(f"\n[ep {case}] y max err {err:.2e}; segments {[sg.cpu().tolist() for sg in segs]}")
     # against the single-GPU forward of the whole layer
-    plan = moe.MoEPlan(T, d, E, k, F, dtype=dtype, tau=tau, has_bias=zipf, path=path)
-    got = parity.run_gpu(plan, dev)
+    plan = moe.MoEPlan(T, d, E, k, F, dtype="bf16", tau=tau, has_bias=zipf, path=path)
+    got = parity.run_gpu(plan, inp.to("cuda"))
     y1 = parity.to_np(got["y"])
-    assert np.max(np.abs(y - y1) / (1 + np.abs(y1))) <= tol
+    assert np.max(np.abs(y - y1) / (1 + np.abs(y1))) <= parity.Y_TOL["bf16"]
+
+
+def test_expert_parallel_degenerate_layouts():
+    """W = 1 (one rank holds every expert: one segment per expert), and W = 2 with a router
+    bias that keeps every token off rank 1's experts (rank 1 receives no rows, its expert
+    stage has an empty tile table, and it sends none back)."""
+    T, d, E, k, F, tau = 256, 256, 8, 2, 128, 1.0
+    s = MoEShape("ep1", T=T, d=d, E=E, k=k, F=F, dtype="bf16", tau=tau)
+    inp = make_inputs(s, seed=9)
+    ranks, y, aux, segs = run_ep(T, d, E, k, F, 1, tau, "auto", inp)
+    check_against_oracle(T, d, E, k, F, tau, inp, ranks, y, aux, full_tokens=True)
+    inp.bias = torch.zeros(E, dtype=torch.float32)
+    inp.bias[E // 2:] = -100.0
+    ranks, y, aux, segs = run_ep(T, d, E, k, F, 2, tau, "auto", inp)
+    assert int(segs[1].sum()) == 0 and int(segs[0].sum()) == T * k
+    check_against_oracle(T, d, E, k, F, tau, inp, ranks, y, aux, full_tokens=True)
 
 
 def test_expert_stage_rejects_counts_beyond_its_rows():

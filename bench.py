@@ -140,7 +140,12 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-i", str(self.dev), "-lms", "100"], stdout=self.file,
                                          stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            # nvidia-smi's first query initialises NVML, which can stall the GPU for a while:
+            # let it finish (the first sample is written) before the timed region starts
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and os.path.getsize(self.file.name) == 0:
+                time.sleep(0.05)
+            time.sleep(0.2)
         except Exception:
             self.proc = None
         return self
@@ -577,7 +582,8 @@ def main():
         g1_flops = 4 * shape.N * shape.d * shape.F  # the dominant kernel: SwiGLU GEMM (W1 and W3)
         g1_tflops = g1_flops / (g1_ms / 1e3) / 1e12
         gemm_tflops = gemm_flops / ((g1_ms + g2_ms) / 1e3) / 1e12
-        traffic = recorded_traffic(shape.name, "gemm1_swiglu")
+        # the committed ncu figure is for the listed layer's full size only
+        traffic = recorded_traffic(shape.name, "gemm1_swiglu") if shape.T == SHAPES[shape.name].T else None
         x_bytes = shape.T * shape.d * 2
         perm_bytes = x_bytes + shape.N * shape.d * 2 + 16 * shape.N
         comb_bytes = shape.N * shape.d * 2 + shape.T * shape.d * 2

@@ -83,6 +83,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, 
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+// the same with an L2 eviction-priority hint
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src), "l"(policy)
+      : "memory");
+}
 // at most one of this thread's bulk groups still reading its shared-memory source
 __device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // all of this thread's bulk groups complete (their global writes performed)
@@ -94,7 +103,8 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // (lane < vw) writes its 128 bytes to dst directly, so that no row of the next expert is
 // touched.  vw is the same for the whole warp.
 __device__ __forceinline__ void store_rows64(const uint32_t (&pk)[32], int vw, int lane, uint32_t stg,
-                                             int& stg_buf, const CUtensorMap* map, int x, int y, void* dst) {
+                                             int& stg_buf, const CUtensorMap* map, int x, int y, void* dst,
+                                             uint64_t policy = 0) {
   if (vw >= 32) {
     const uint32_t blk = stg + (uint32_t)(stg_buf * kStgBlockBytes);
     if (lane == 0) bulk_wait_read_le1();  // the store issued from this block two blocks ago has read it
@@ -105,13 +115,44 @@ __device__ __forceinline__ void store_rows64(const uint32_t (&pk)[32], int vw, i
                    pk[4 * j + 3]);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA engine
     __syncwarp();
-    if (lane == 0) tma_store_2d(map, x, y, blk);
+    if (lane == 0) {
+      if (policy != 0)
+        tma_store_2d_hint(map, x, y, blk, policy);
+      else
+        tma_store_2d(map, x, y, blk);
+    }
     stg_buf ^= 1;
   } else if (lane < vw) {
     uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int v = 0; v < 8; ++v) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
   }
+}
+
+// L2 eviction priority of the SwiGLU GEMM's operand loads and H stores (0: the default,
+// 1: evict_last, 2: evict_first).  A scheduling group's A rows are read once per n-tile, so
+// they are kept (evict_last); H is not read again by this kernel (evict_first); each weight
+// n-tile is read by the group's pairs one after another and keeps the default priority (as
+// evict_first the weights were read from DRAM about three times over).
+constexpr int kHintA = 1;
+constexpr int kHintB = 0;
+constexpr int kHintY = 2;
+
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+  uint64_t p = 0;
+  if (hint == 1) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  if (hint == 2) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d_pair with an L2 eviction-priority hint
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                      uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ void raise_abort(Ctl2* ctl, uint32_t rank) {
@@ -188,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true, first = true;
       const CUtensorMap* bmap = (kMode == 1 && rank == 1) ? &tmB3 : &tmB;
+      const uint64_t pol_a = l2_policy(kMode == 1 ? kHintA : 0), pol_b = l2_policy(kMode == 1 ? kHintB : 0);
       for (int tile = cid; tile < total && ok; tile += ncl) {
         const TileInfo ti = decode_pair_tile(ws, n_tiles, tile, (int)rank);
         const int brow = kMode == 1 ? ti.e * s.F + ti.n_idx * bn : ti.e * s.d + ti.n_idx * bn + (int)rank * (kMmaN / 2);
@@ -201,8 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) ptx::mbar_arrive_expect_tx(full_local, 2 * kStageBytes);
             const uint32_t bar = ptx::mapa(full_local, 0);
             const uint32_t sa = ptx::smem_u32(stages + (size_t)stage * kStageBytes);
-            ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, ti.row0, bar);
-            ptx::tma_load_2d_pair(sa + kABytes, bmap, kb * kBK, brow, bar);
+            if (kMode == 1 && kHintA != 0)
+              tma_load_2d_pair_hint(sa, &tmA, kb * kBK, ti.row0, bar, pol_a);
+            else
+              ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, ti.row0, bar);
+            if (kMode == 1 && kHintB != 0)
+              tma_load_2d_pair_hint(sa + kABytes, bmap, kb * kBK, brow, bar, pol_b);
+            else
+              ptx::tma_load_2d_pair(sa + kABytes, bmap, kb * kBK, brow, bar);
           }
           first = false;
           if (++stage == kStages) {
@@ -268,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t stg = ptx::smem_u32(stg_base) + (uint32_t)(q * 2 * kStgBlockBytes);
     int stg_buf = 0;  // the staging block of this warp's next tiled store
+    const uint64_t pol_y = l2_policy(kMode == 1 ? kHintY : 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -318,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          store_rows64(pk, vw, lane, stg, stg_buf, &tmY, n0 + c, ti.row0 + q * 32, hrow + c);
+          store_rows64(pk, vw, lane, stg, stg_buf, &tmY, n0 + c, ti.row0 + q * 32, hrow + c, pol_y);
         }
       } else {
         const float gate = valid ? ws.gate_perm[p] : 0.f;

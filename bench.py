@@ -235,13 +235,14 @@ def measure_shape(shape, steps, warmup):
         plan.forward(*a)
         evs[i][1].record()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(steps)]
-    for i in range(steps):
-        flush.zero_()
-        for s_ in range(len(STAGES)):
-            ev[i][s_].record()
-            plan.forward_stage(s_, *a)
-        ev[i][len(STAGES)].record()
-    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(steps):
+            flush.zero_()
+            for s_ in range(len(STAGES)):
+                ev[i][s_].record()
+                plan.forward_stage(s_, *a)
+            ev[i][len(STAGES)].record()
+        torch.cuda.synchronize()
     if plan.device_status(ws) != 0:
         raise RuntimeError(f"device status error on {shape.name}")
     step_ms = sum(b.elapsed_time(e) for b, e in evs) / steps
@@ -251,7 +252,8 @@ def measure_shape(shape, steps, warmup):
     g_ms = stage_ms["gemm1_swiglu"] + stage_ms["gemm2_gate"]
     out = {"workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k, "d_expert": shape.F,
            "G": None, "tokens_per_s": shape.T / (step_ms / 1e3), "ms_per_step": step_ms,
-           "grouped_gemm_tflops": shape.expert_flops / (g_ms / 1e3) / 1e12, "stage_ms": stage_ms, "counts": counts}
+           "grouped_gemm_tflops": shape.expert_flops / (g_ms / 1e3) / 1e12, "stage_ms": stage_ms, "counts": counts,
+           "clocks": clk.summary()}
     del dev, plan, ws, y, flush
     torch.cuda.empty_cache()
     return out
@@ -278,23 +280,34 @@ def run_perf_model(args):
     train = [SHAPES[n] for n in ("coarse_e8", "fine_e32", "skewed_e128", "large_e64")]
     test = granularity_sweep()
     meas = {sh.name: measure_shape(sh, steps, args.warmup) for sh in train + test}
-    samples = [(pm.features(sh, meas[sh.name]["counts"]), meas[sh.name]["stage_ms"]) for sh in train]
+    mhz = {n: m["clocks"]["sm_mhz"] for n, m in meas.items()}
+    feats = {sh.name: pm.features(sh, meas[sh.name]["counts"], sm_mhz=mhz[sh.name]) for sh in train + test}
+    samples = [(feats[sh.name], meas[sh.name]["stage_ms"]) for sh in train]
     params = pm.fit(samples)
+    # the same model without the clock term, for comparison
+    feats0 = {sh.name: pm.features(sh, meas[sh.name]["counts"]) for sh in train + test}
+    params0 = pm.fit([(feats0[sh.name], meas[sh.name]["stage_ms"]) for sh in train])
     report = []
     for sh in train + test:
         m = dict(meas[sh.name]["stage_ms"])
         m["total"] = sum(m[st] for st in pm.STAGES)
-        pred = pm.predict(params, pm.features(sh, meas[sh.name]["counts"]))
+        pred = pm.predict(params, feats[sh.name])
         err = pm.mape(pred, m)
-        report.append({"workload": sh.name, "role": "fit" if sh in train else "held out",
+        err0 = pm.mape(pm.predict(params0, feats0[sh.name]), m)
+        report.append({"workload": sh.name, "role": "fit" if sh in train else "held out", "sm_mhz": mhz[sh.name],
+                       "total_err_pct_without_clock": round(100 * err0["total"], 2),
                        "measured_ms": {k: round(v, 4) for k, v in m.items()},
                        "predicted_ms": {k: round(v, 4) for k, v in pred.items()},
                        "abs_pct_err": {k: round(100 * v, 2) for k, v in err.items()}})
     held = [r for r in report if r["role"] == "held out"]
-    print(json.dumps({"perf_model": "t = L + work / rate per kernel, fitted on the four listed bf16 workloads",
+    print(json.dumps({"perf_model": "t = L + work / rate per kernel, fitted on the four listed bf16 workloads; "
+                                    "GEMM work counted at the reference SM clock (work * 2070 MHz / the layer's "
+                                    "median SM clock)",
                       "params": {st: {"L_ms": round(L, 5), "per_unit_ms": slope} for st, (L, slope) in params.items()},
                       "fitted_rates": pm.rates(params),
                       "held_out_total_mape_pct": round(sum(r["abs_pct_err"]["total"] for r in held) / len(held), 2),
+                      "held_out_total_mape_pct_without_clock":
+                          round(sum(r["total_err_pct_without_clock"] for r in held) / len(held), 2),
                       "rows": report}), flush=True)
 
 

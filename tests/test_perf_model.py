@@ -92,6 +92,22 @@ def test_features_charge_padding_and_the_last_wave():
     assert f["route"] == s.T * s.d * 2 + s.N * 8
 
 
+def test_features_count_gemm_work_at_the_reference_clock():
+    """A layer that ran at a lower SM clock carries proportionally more GEMM work (the tensor
+    cores' rate scales with the clock); the movers' bytes do not depend on it."""
+    s = SHAPES["large_e64"]
+    counts = [s.N // s.E] * s.E
+    f = pm.features(s, counts)
+    f_max = pm.features(s, counts, sm_mhz=pm.REF_MHZ)
+    f_cap = pm.features(s, counts, sm_mhz=pm.REF_MHZ / 1.25)
+    for st in pm.STAGES:
+        assert f_max[st] == pytest.approx(f[st])
+    for st in ("gemm1_swiglu", "gemm2_gate"):
+        assert f_cap[st] == pytest.approx(1.25 * f[st])
+    for st in ("route", "permute", "combine"):
+        assert f_cap[st] == f[st]
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape", [SHAPES[n] for n in ORDER[1:]] + granularity_sweep(), ids=lambda s: s.name)
 def test_pair_tiles_match_the_scan_kernel(shape):

@@ -10,9 +10,12 @@ kernels of this library, from quantities the layer shape and the routing fix:
 
 FLOP_padded counts the rows the tensor cores actually process (256-row CTA-pair tiles of
 each expert, so padding and odd m-tiles count), and wave_efficiency = tiles / (slots *
-ceil(tiles / slots)) charges the last partial wave of the persistent grid.  L, B, R are
-fitted per kernel by least squares on measured stage times (fit), then used to predict
-others (predict); mape() reports the mean absolute percentage error.
+ceil(tiles / slots)) charges the last partial wave of the persistent grid.  The tensor-core
+rate scales with the SM clock, which the 1.4 kW power cap pulls down on the largest layers:
+given the median SM clock f seen while a layer ran, the GEMM work is counted at the reference
+clock, FLOP_padded * f_ref / f.  L, B, R are fitted per kernel by least squares on measured
+stage times (fit), then used to predict others (predict); mape() reports the mean absolute
+percentage error.
 """
 import math
 
@@ -36,9 +39,12 @@ def pair_tiles(counts):
     return pairs
 
 
-def features(shape, counts, slots=76):
-    """Per-stage (work, extra) features of one forward: bytes for movers, padded FLOPs and
-    wave efficiency for the GEMMs."""
+REF_MHZ = 2070.0  # the GB300's maximum SM clock
+
+
+def features(shape, counts, slots=76, sm_mhz=None):
+    """Per-stage work of one forward: bytes for movers, padded FLOPs over the wave efficiency
+    for the GEMMs, counted at REF_MHZ when the layer's SM clock sm_mhz is given."""
     T, d, E, k, F = shape.T, shape.d, shape.E, shape.k, shape.F
     N = T * k
     pairs = pair_tiles(counts)
@@ -46,11 +52,12 @@ def features(shape, counts, slots=76):
     t1 = pairs * math.ceil(F / GEMM1_TILE_N)
     t2 = pairs * math.ceil(d / GEMM2_TILE_N)
     wave = lambda n: n / (slots * math.ceil(n / slots)) if n else 1.0
+    clk = REF_MHZ / sm_mhz if sm_mhz else 1.0
     return {
         "route": T * d * 2 + N * 8,
         "permute": T * d * 2 + N * d * 2 + 28 * N,
-        "gemm1_swiglu": 4.0 * rows * d * F / wave(t1),
-        "gemm2_gate": 2.0 * rows * d * F / wave(t2),
+        "gemm1_swiglu": 4.0 * rows * d * F / wave(t1) * clk,
+        "gemm2_gate": 2.0 * rows * d * F / wave(t2) * clk,
         "combine": N * d * 2 + T * d * 2,
     }
 

@@ -95,6 +95,22 @@ def test_all_tokens_to_one_expert(moe, path):
 
 
 @pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T", [2048, 2049, 2176, 2304, 4097])
+def test_scheduling_group_boundaries(moe, path, T):
+    """k = 1 and a +100 logit bias on expert 0: all T rows in one expert, so its m-tiles (128
+    rows) fill scheduling groups of 16 exactly (T = 2048), spill one row into a second group
+    (2049: a half-empty pair of one row), fill a 17th m-tile (2176: an odd group of one full
+    m-tile), an 18th (2304: a whole second pair) or a third group (4097).  Every row of H, Yp
+    and y is compared."""
+    s = small("groups", T, 128, 4, 1, 64)
+    inp = make_inputs(s, seed=7)
+    inp.bias = torch.zeros(s.E, dtype=torch.float32)
+    inp.bias[0] = 100.0
+    rep, got = check(moe, s, inp, path=path)
+    assert got["views"]["expert_counts"][0].item() == T
+
+
+@pytest.mark.parametrize("path", PATHS)
 def test_uniform_router_aux_is_one(moe, path):
     """W_r = 0: every logit equal, p = 1/E; the balancing scalar is exactly 1 (k slots
     always sum to 1 whatever the tie-break) and top-k takes the lowest indices."""

@@ -163,3 +163,52 @@ def test_backward_full_size_coarse_e8():
     for n in names:
         assert errs[n] <= TOL, f"{n}: {errs[n]}"
         assert nerrs[n] <= NORM_TOL, f"{n}: norm-wise {nerrs[n]}"
+
+
+def draw_backward_case(i):
+    rng = np.random.default_rng(3000 + i)
+    E = int(rng.choice([1, 2, 4, 8, 16]))
+    return dict(T=int(rng.choice([100, 257, 384, 640, 900])), d=int(rng.choice([64, 128, 256, 384, 512])),
+                E=E, k=int(rng.integers(1, min(E, 4) + 1)), F=int(rng.choice([64, 128, 192, 320, 384])),
+                alpha=float(rng.choice([0.0, 0.1, 0.5])), renorm=bool(rng.integers(0, 2)),
+                bias=bool(rng.integers(0, 2)), tau=float(rng.choice([0.5, 1.0, 2.0])),
+                path=["auto", "tc1"][i % 2])
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_backward_random_shapes(i):
+    """Seeded random shapes, temperatures, router biases, gate variants, balancing-loss weights
+    and GEMM paths; the inputs' seed is the first (from 40) whose routing is clear of near-ties
+    in the oracle, so that the gradients follow the oracle's own routing.  Every element of every
+    gradient is compared."""
+    from top_routing_grouped_gb300 import moe
+    import parity
+    c = draw_backward_case(i)
+    T, d, E, k, F = c["T"], c["d"], c["E"], c["k"], c["F"]
+    s = MoEShape(f"bwd_random{i}", T=T, d=d, E=E, k=k, F=F, dtype="bf16", tau=c["tau"], renorm=c["renorm"])
+    orc = oracle.Oracle(T, d, E, k, F, tau=s.tau, dtype="bf16", renorm=c["renorm"])
+    for seed in range(40, 80):
+        inp = make_inputs(s, seed=seed)
+        inp.bias = torch.linspace(-0.4, 0.4, E, dtype=torch.float32) if c["bias"] else None
+        host = inp.numpy_for_oracle()
+        z, _, oidx, _ = orc.router(host["x"], host["wr"], host["bias"])
+        if parity.clear_tokens(z, k).all():
+            break
+    else:
+        pytest.fail("no seed with routing clear of near-ties")
+    plan, ws, dy, got = run_backward(moe, s, inp, c["alpha"], path=c["path"])
+    np.testing.assert_array_equal(np.sort(plan.views(ws)["topk_idx"].cpu().numpy(), 1), np.sort(oidx, 1))
+    ref = orc.backward(host["x"], host["wr"], host["bias"], host["w1"], host["w3"], host["w2"],
+                       dy.float().numpy().astype(np.float64), c["alpha"])
+    names = ["dx", "dwr", "dw1", "dw3", "dw2"] + (["dbias"] if c["bias"] else [])
+    # one expert: the softmax is constant, so the router's gradients are exactly zero
+    zero = [n for n in names if not np.any(ref[n])]
+    for n in zero:
+        assert not np.any(got[n]), f"{n} should be zero"
+    names = [n for n in names if n not in zero]
+    errs = {n: rel_err(got[n], ref[n]) for n in names}
+    nerrs = {n: norm_err(got[n], ref[n]) for n in names}
+    print(f"\n[backward random {c} seed={seed}] " + " ".join(f"{n}={errs[n]:.2e}/{nerrs[n]:.2e}" for n in names))
+    for n in names:
+        assert errs[n] <= TOL, f"{n}: {errs[n]}"
+        assert nerrs[n] <= NORM_TOL, f"{n}: norm-wise {nerrs[n]}"

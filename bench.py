@@ -50,6 +50,8 @@ def parse():
                     help="time the training step: forward (keeping activations) + backward")
     ap.add_argument("--perf-model", action="store_true",
                     help="fit the operator-level model on the listed workloads, predict the sweep")
+    ap.add_argument("--ep-stage", type=int, default=0, metavar="W",
+                    help="time the expert-parallel expert stage of W ranks emulated on this GPU")
     return ap.parse_args()
 
 
@@ -413,10 +415,80 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_ep_stage(args):
+    """The expert stage of expert parallelism (moe_expert_forward: segment scan + the grouped
+    SwiGLU GEMM and down-projection over the rows a rank receives), for W ranks emulated on this
+    GPU: every rank routes and dispatches its token slice, the row all-to-all is done by copies,
+    then each rank's expert stage is timed alone (CUDA events, L2 flushed before each step).
+    Beside it, the same layer's two GEMMs in the single-GPU forward (staged events), which
+    multiply the same rows without the per-source segments."""
+    import torch
+    from top_routing_grouped_gb300 import moe
+    from top_routing_grouped_gb300.ep import EPRank, rows_per_rank
+    from top_routing_grouped_gb300.workloads import SHAPES, make_inputs
+    shape = SHAPES[args.workload]
+    W = args.ep_stage
+    if shape.T % W or shape.E % W:
+        raise SystemExit(f"{shape.name}: T and E must split evenly over {W} ranks")
+    dev = make_inputs(shape, seed=0).to("cuda")
+    Tl, El = shape.T // W, shape.E // W
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    ranks = [EPRank(Tl, shape.d, shape.E, shape.k, shape.F, W, r, tau=shape.tau, has_bias=shape.zipf_bias,
+                    renorm_gates=shape.renorm) for r in range(W)]
+    xs = [dev.x[r * Tl:(r + 1) * Tl].contiguous() for r in range(W)]
+    ys = [torch.empty(Tl, shape.d, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+    wl = [(dev.w1[r * El:(r + 1) * El].contiguous(), dev.w3[r * El:(r + 1) * El].contiguous(),
+           dev.w2[r * El:(r + 1) * El].contiguous()) for r in range(W)]
+    for r, rk in enumerate(ranks):
+        rk.dispatch(xs[r], dev.w_router, dev.bias, ys[r])
+    counts = [rk.counts().cpu() for rk in ranks]
+    segs = [torch.cat([counts[j][r * El:(r + 1) * El] for j in range(W)]).cuda() for r in range(W)]
+    send = [rows_per_rank(counts[r], W) for r in range(W)]
+    for j in range(W):  # the row and gate all-to-alls, as copies
+        for dst, src in ((ranks[j].x_recv, "xp"), (ranks[j].g_recv, "gate_perm")):
+            parts = [ranks[r].views[src][sum(send[r][:j]):sum(send[r][:j + 1])] for r in range(W)]
+            cat = torch.cat(parts)
+            dst[:cat.shape[0]].copy_(cat)
+    per_rank = []
+    for r, rk in enumerate(ranks):
+        for _ in range(args.warmup):
+            rk.experts(segs[r], *wl[r])
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record()
+            rk.experts(segs[r], *wl[r])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if rk.exp.device_status(rk.ws_exp) != moe.MOE_OK:
+            raise RuntimeError(f"device status error in rank {r}'s expert stage")
+        per_rank.append(sum(a.elapsed_time(b) for a, b in ev) / args.steps)
+    rows = [int(sg.sum()) for sg in segs]
+    seg_rows = [sg.cpu().tolist() for sg in segs]
+    exec_rows = [128 * sum((c + 127) // 128 for c in sr) for sr in seg_rows]
+    del ranks
+    torch.cuda.empty_cache()
+    single = measure_shape(shape, max(10, args.steps // 5), args.warmup)
+    g_single = single["stage_ms"]["gemm1_swiglu"] + single["stage_ms"]["gemm2_gate"]
+    flops = shape.expert_flops
+    print(json.dumps({
+        "ep_stage": {"workload": shape.name, "ranks": W, "tokens_per_rank": Tl, "experts_per_rank": El,
+                     "rows_per_rank": rows, "m_tile_rows_per_rank": exec_rows,
+                     "expert_stage_ms_per_rank": [round(t, 4) for t in per_rank],
+                     "sum_ms": round(sum(per_rank), 4), "max_ms": round(max(per_rank), 4),
+                     "single_gpu_gemms_ms": round(g_single, 4),
+                     "sum_tflops": flops / (sum(per_rank) / 1e3) / 1e12,
+                     "single_gpu_gemm_tflops": flops / (g_single / 1e3) / 1e12,
+                     "from": "CUDA events around moe_expert_forward per rank (ranks emulated on one GPU, "
+                             "all-to-alls by copies); single-GPU GEMMs from the staged forward"}}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.ep_stage:
+        return run_ep_stage(args)
     if args.sweep:
         return run_sweep(args)
     if args.perf_model:
